@@ -1,0 +1,64 @@
+"""NumPy fp64 restatement of the attention forward: a second, independent oracle for small cases.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``). It is written with whole-matrix NumPy
+operations, unlike the C oracle's scalar loops, so that a slip in one restatement shows up as a
+disagreement with the other.
+
+Definition followed (the standard_attention listings on "AI训练的最大障碍不是算力,而是'内存墙'"
+(zsdodo.com) and "闪电注意力：革命性地提高Transformer效率" (unite.ai); the max-subtracted softmax of
+formula 1 in the latter's section "闪电注意力的数学原理"; padded keys ignored as in
+"基于AIFI多头注意力机制的高效序列建模实战", "动态序列处理"; grouped heads as in the unite.ai section
+"闪电注意力-2"):
+
+    S = scale * Q K^T over the key axis, masked entries set to -inf,
+    P = softmax(S) row-wise with the row maximum subtracted,
+    O = P V,  LSE = m + ln(sum exp(S - m)).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def key_mask(N: int, causal: bool, kv_len: int) -> np.ndarray:
+    """Boolean [N, N] matrix: True where query i may attend to key j."""
+    j = np.arange(N)[None, :]
+    i = np.arange(N)[:, None]
+    ok = j < max(0, min(int(kv_len), N))
+    if causal:
+        ok = ok & (j <= i)
+    return np.broadcast_to(ok, (N, N))
+
+
+def attention_np(q, k, v, scale, causal=False, kv_len=None, return_p=False):
+    """q [B,H,N,d], k/v [B,H_kv,N,d] (any float dtype, upcast to fp64). Returns O, LSE (and P)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    assert H % H_kv == 0
+    g = H // H_kv
+    O = np.zeros((B, H, N, d))
+    LSE = np.zeros((B, H, N))
+    P_all = np.zeros((B, H, N, N)) if return_p else None
+    for b in range(B):
+        L = N if kv_len is None else int(kv_len[b])
+        mask = key_mask(N, causal, L)
+        for h in range(H):
+            kh = h // g
+            S = float(scale) * (q[b, h] @ k[b, kh].T)
+            S = np.where(mask, S, -np.inf)
+            m = S.max(axis=1)
+            has = np.isfinite(m)
+            m_safe = np.where(has, m, 0.0)
+            E = np.exp(S - m_safe[:, None])  # exp(-inf) = 0 on masked entries
+            l = E.sum(axis=1)
+            P = np.where(has[:, None], E / np.where(has, l, 1.0)[:, None], 0.0)
+            O[b, h] = P @ v[b, kh]
+            with np.errstate(divide="ignore"):
+                LSE[b, h] = np.where(has, m_safe + np.log(np.where(has, l, 1.0)), -np.inf)
+            if return_p:
+                P_all[b, h] = P
+    if return_p:
+        return O, LSE, P_all
+    return O, LSE
