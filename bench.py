@@ -1,0 +1,314 @@
+"""Benchmark of the attention forward on B300: one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one attn_fwd call (V -> fp16 pre-pass + the tensor-core attention kernel) over the whole
+workload, inputs resident in HBM. Default workload: B=1, H=16, N=8192, d=128, bf16, non-causal,
+1% of key rows scaled x8 (the headline N=8192, d=128 point). L2 is flushed (256 MiB write) before
+every timed step, outside the timed events. Under torchrun each rank runs the same workload on its
+own GPU (independent problems, no collective on the data path) and the max time over ranks counts.
+
+``--impl reference`` times the fp64 CPU oracle instead (the only reference implementation available:
+the pages ship no runnable code), on a bounded sample of the workload's query rows per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_tiled_attention_50_b300 import inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s and % of B300 dense-BF16 peak at N=8192, d=128"
+UNIT = "TFLOP/s"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(bf16=float(d["bf16_tflops"]), bf16_sustained=float(d["bf16_tflops_sustained"]),
+                    hbm=float(d["hbm_gbs"]), source="measured")
+    return dict(bf16=1800.0, bf16_sustained=1400.0, hbm=6400.0, source="fallback")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            self.t0 = time.time()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(r[1]) for r in rows]
+        mx = [num(r[2]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(rows), "reasons": reasons,
+                "power_w_max": max(num(r[3]) for r in rows)}
+
+
+def flops_of(w) -> float:
+    return w.nominal_flops()
+
+
+def oracle_sample_rows(w, n_rows, seed=0):
+    rng = np.random.default_rng(seed)
+    total = w.B * w.H * w.N
+    return np.sort(rng.choice(total, size=min(n_rows, total), replace=False)).astype(np.int64)
+
+
+def time_oracle(x, w, rows_per_step, steps, warmup):
+    """The fp64 CPU oracle (as it stands) on `rows_per_step` query rows per step."""
+    import oracle
+    per_row = 4.0 * w.N * w.d * (0.5 if w.causal else 1.0)  # nominal FLOPs of one query row
+    times = []
+    for s in range(warmup + steps):
+        rows = oracle_sample_rows(w, rows_per_step, seed=s)
+        t0 = time.perf_counter()
+        oracle.attention_rows(x.q, x.k, x.v, x.scale, rows, causal=w.causal, kv_len=x.kv_len)
+        dt = time.perf_counter() - t0
+        if s >= warmup:
+            times.append(dt)
+    sec = sum(times) / len(times)
+    return dict(value=per_row * rows_per_step / sec / 1e12, sec_per_step=sec, cores=oracle.num_threads(),
+                sample=f"{rows_per_step} query rows (of {w.B * w.H * w.N}) of {w.name} per step, each row over all "
+                       f"{w.N} keys in fp64")
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    x = inputs.make_inputs(w)
+    r = time_oracle(x, w, args.ref_rows, args.steps, args.warmup)
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["sec_per_step"] * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, on the host)",
+        "impl": "reference",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d, "causal": w.causal,
+                   "sample_rows_per_step": args.ref_rows},
+        "cpu_baseline": {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": r["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from exact_tiled_attention_50_b300 import attn
+
+    x = inputs.make_inputs(w)
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    kv = x.kv_len.to(dev) if x.kv_len is not None else None
+    B, H, N, d = q.shape
+    out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    wsb = attn.workspace_bytes(B, w.H, w.H_kv, N, d, q.dtype)
+    work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        attn.attn_fwd(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, out=out, lse=lse, workspace=work)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    rc = attn.check()
+    if rc != attn.ATTN_OK:
+        raise RuntimeError(f"warm-up failed: {attn.status_string(rc)}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in kev:  # torch creates the CUDA event on first record: materialise the handles now
+        a.record(stream)
+        b.record(stream)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()  # outside the timed events: evicts Q/K/V/O from L2
+        attn.set_kernel_events(*kev[i])
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    attn.set_kernel_events(None, None)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    rc = attn.check()
+    if rc != attn.ATTN_OK:
+        raise RuntimeError(f"timed run failed: {attn.status_string(rc)}")
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    kern_ms = sum(attn.event_elapsed_ms(a, b) for a, b in kev) / K
+    if ws > 1:
+        t = torch.tensor([step_ms, kern_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms, kern_ms = float(t[0]), float(t[1])
+
+    # ---- end to end through the public API: pinned host inputs -> device -> attn_fwd -> host ----
+    hq, hk, hv = x.q.pin_memory(), x.k.pin_memory(), x.v.pin_memory()
+    hkv = x.kv_len.pin_memory() if x.kv_len is not None else None
+    ho = torch.empty_like(out, device="cpu").pin_memory()
+    hl = torch.empty_like(lse, device="cpu").pin_memory()
+    e2e_steps = max(1, min(K, args.e2e_steps))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(e2e_steps + 1):
+        flush.zero_()
+        e0.record(stream)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        if hkv is not None:
+            kv.copy_(hkv, non_blocking=True)
+        step()
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i > 0:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e = sum(e2e_ms) / len(e2e_ms)
+    if ws > 1:
+        t = torch.tensor([e2e], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e = float(t[0])
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv)) + (hkv.numel() * 4 if hkv is not None else 0)
+    d2h = ho.numel() * 4 + hl.numel() * 4
+
+    flops = flops_of(w)
+    peaks = load_peaks()
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": ws * flops / (step_ms * 1e-3) / 1e12,
+        "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), 1% of key rows x8)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d, "causal": w.causal,
+                   "in": "bf16", "out": "fp32 O + fp32 LSE",
+                   "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
+                   "parallelism": f"replicas x{ws} (independent problems per GPU)",
+                   "pct_of_peak_bf16": 100.0 * flops / (step_ms * 1e-3) / 1e12 / peaks["bf16"]},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": UNIT,
+                     "frac": achieved / peaks["bf16"], "traffic": args.traffic,
+                     "kernel": "attn_fwd_tc_kernel<128,false>", "kernel_ms": kern_ms,
+                     "peak_source": f"{peaks['source']} bf16 burst (cuBLAS); "
+                                    f"frac of sustained {achieved / peaks['bf16_sustained']:.3f}"},
+        "e2e": {"value": ws * flops / (e2e * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
+        "gpu_launches": K * attn.launches_per_call(q.dtype),
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        r = time_oracle(x, w, args.ref_rows, 1, 0)
+        line["cpu_baseline"] = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                                "sample": r["sample"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--ref-rows", type=int, default=1024, help="oracle query rows per step (reference / cpu leg)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--traffic", type=float, default=None, help="DRAM bytes per launch from an ncu capture")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,153 @@
+"""Python binding of libattn.so (argument marshalling only; every step runs in the CUDA kernels).
+
+Importing this module loads the in-tree ``libattn.so`` and raises if it is missing: there is no
+fallback implementation. Tensors are torch CUDA tensors (torch provides device memory and streams).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+ATTN_F32, ATTN_BF16 = 0, 1
+
+EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_workspace_bytes", "attn_launches_per_call",
+            "attn_debug_set_wait_limit_ns", "attn_debug_set_skip_kv_load", "attn_set_kernel_events",
+            "attn_event_elapsed_ms")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m exact_tiled_attention_50_b300.build` "
+                          "(there is no CPU or PyTorch fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci, ci, vp, sz, vp]
+    lib.attn_fwd.restype = ci
+    lib.attn_check.argtypes = [vp]
+    lib.attn_check.restype = ci
+    lib.attn_status_string.argtypes = [ci]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_workspace_bytes.argtypes = [ci, ci, ci, ci, ci, ci]
+    lib.attn_workspace_bytes.restype = sz
+    lib.attn_launches_per_call.argtypes = [ci]
+    lib.attn_launches_per_call.restype = ci
+    lib.attn_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.attn_debug_set_wait_limit_ns.restype = None
+    lib.attn_debug_set_skip_kv_load.argtypes = [ci]
+    lib.attn_debug_set_skip_kv_load.restype = None
+    lib.attn_set_kernel_events.argtypes = [vp, vp]
+    lib.attn_set_kernel_events.restype = None
+    lib.attn_event_elapsed_ms.argtypes = [vp, vp]
+    lib.attn_event_elapsed_ms.restype = ctypes.c_float
+    return lib
+
+
+lib = _load()
+
+
+def status_string(code: int) -> str:
+    return lib.attn_status_string(int(code)).decode()
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return ATTN_F32
+    if t == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def workspace_bytes(B: int, H: int, H_kv: int, N: int, d: int, in_dtype: torch.dtype) -> int:
+    return int(lib.attn_workspace_bytes(B, H, H_kv, N, d, _dtype_code(in_dtype)))
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(nbytes: int, device: torch.device) -> torch.Tensor:
+    """A cached device workspace per (device, stream); torch allocations are 256-byte aligned."""
+    key = (device, torch.cuda.current_stream(device).cuda_stream)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[float] = None,
+             causal: bool = False, kv_len: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+             lse: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
+             workspace: Optional[torch.Tensor] = None, want_lse: bool = True):
+    """O, LSE = softmax(scale q k^T) v on the current CUDA stream.
+
+    q [B,H,N,d], k/v [B,H_kv,N,d] (bf16 or fp32, contiguous, on one CUDA device); kv_len int32 [B]
+    on the device or None. Returns (O [B,H,N,d] in out_dtype, LSE [B,H,N] fp32 or None).
+    """
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if k.shape != (B, H_kv, N, d) or v.shape != (B, H_kv, N, d):
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=out_dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if kv_len is not None:
+        kv_len = kv_len.to(device=q.device, dtype=torch.int32).contiguous()
+    ws_bytes = workspace_bytes(B, H, H_kv, N, d, q.dtype)
+    if workspace is None and ws_bytes > 0:
+        workspace = _workspace(ws_bytes, q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                      lse.data_ptr() if lse is not None else None, B, H, H_kv, N, d, float(scale), int(bool(causal)),
+                      kv_len.data_ptr() if kv_len is not None else None, _dtype_code(q.dtype), _dtype_code(out.dtype),
+                      workspace.data_ptr() if workspace is not None else None,
+                      workspace.numel() * workspace.element_size() if workspace is not None else 0, stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def check(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise the stream and return (and clear) the device error status (ATTN_OK on success)."""
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    return int(lib.attn_check(s))
+
+
+def launches_per_call(in_dtype: torch.dtype) -> int:
+    return int(lib.attn_launches_per_call(_dtype_code(in_dtype)))
+
+
+def set_kernel_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]) -> None:
+    """Record ``start``/``stop`` around the main attention kernel of every following call (None: off)."""
+    if start is None or stop is None:
+        lib.attn_set_kernel_events(None, None)
+    else:
+        lib.attn_set_kernel_events(start.cuda_event, stop.cuda_event)
+
+
+def event_elapsed_ms(start: torch.cuda.Event, stop: torch.cuda.Event) -> float:
+    """Elapsed time between two events recorded by the library's timing hook."""
+    ms = float(lib.attn_event_elapsed_ms(start.cuda_event, stop.cuda_event))
+    if ms < 0:
+        raise RuntimeError("cudaEventElapsedTime failed")
+    return ms

@@ -1,0 +1,197 @@
+// C ABI front end of libattn.so: argument validation, workspace layout, TMA tensor maps, dispatch.
+// The operation, layouts and error conventions are documented in include/attn.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+
+namespace {
+
+constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;  // 1 s
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_skip_kv_load{0};
+std::atomic<cudaEvent_t> g_ev_start{nullptr};
+std::atomic<cudaEvent_t> g_ev_stop{nullptr};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WorkspaceLayout {
+    size_t v16 = 0, partial = 0, vexp = 0, total = 0;
+    int chunks = 0;
+};
+
+bool workspace_layout(int B, int H_kv, int N, int d, WorkspaceLayout* w) {
+    const long long elems_per_head = static_cast<long long>(N) * d;
+    const long long heads = static_cast<long long>(B) * H_kv;
+    w->chunks = static_cast<int>((elems_per_head + attn_impl::VPREP_CHUNK - 1) / attn_impl::VPREP_CHUNK);
+    w->v16 = 0;
+    w->partial = round_up(static_cast<size_t>(heads * elems_per_head) * 2, 256);
+    w->vexp = w->partial + round_up(static_cast<size_t>(heads) * w->chunks * sizeof(float), 256);
+    w->total = w->vexp + round_up(static_cast<size_t>(heads) * sizeof(int32_t), 256);
+    return w->chunks <= 65535 && heads <= 65535;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// 3-D map over [slabs, rows, d] 16-bit values: box of 64 columns x 128 rows, 128-byte swizzle,
+// rows past `rows` in a slab read as zero.
+bool encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int d, int rows, long long slabs) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(slabs)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool sizes_ok(int B, int H, int H_kv, int N, int d) {
+    if (B <= 0 || H <= 0 || H_kv <= 0 || N <= 0) return false;
+    if (H % H_kv != 0) return false;
+    if (d != 64 && d != 128) return false;
+    if (static_cast<long long>(B) * H > 0x7fffffffLL / 2) return false;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_workspace_bytes(int B, int H, int H_kv, int N, int d, attn_dtype in_dtype) {
+    if (!sizes_ok(B, H, H_kv, N, d)) return 0;
+    if (in_dtype != ATTN_BF16) return 0;
+    WorkspaceLayout w;
+    if (!workspace_layout(B, H_kv, N, d, &w)) return 0;
+    return w.total;
+}
+
+attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
+                     int N, int d, float scale, int causal, const int32_t* kv_len, attn_dtype in_dtype,
+                     attn_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!Q || !K || !V || !O) return ATTN_ERR_INVALID_ARG;
+    if (!sizes_ok(B, H, H_kv, N, d)) return ATTN_ERR_INVALID_ARG;
+    if (!(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return ATTN_ERR_INVALID_ARG;
+    if (LSE && !aligned(LSE, 4)) return ATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return ATTN_ERR_INVALID_ARG;
+    if (in_dtype != ATTN_F32 && in_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (out_dtype != ATTN_F32 && out_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+
+    if (in_dtype == ATTN_F32) {
+        if (out_dtype != ATTN_F32) return ATTN_ERR_UNSUPPORTED;
+        if (static_cast<long long>(B) * H > 65535) return ATTN_ERR_UNSUPPORTED;
+        attn_impl::F32Params p{};
+        p.Q = static_cast<const float*>(Q);
+        p.K = static_cast<const float*>(K);
+        p.V = static_cast<const float*>(V);
+        p.O = O;
+        p.LSE = LSE;
+        p.kv_len = kv_len;
+        p.B = B; p.H = H; p.H_kv = H_kv; p.N = N; p.group = H / H_kv; p.causal = causal;
+        p.scale = scale;
+        return attn_impl::launch_attn_f32(d, p, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    }
+
+    // bf16 inputs: tensor-core path
+    WorkspaceLayout w;
+    if (!workspace_layout(B, H_kv, N, d, &w)) return ATTN_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total) return ATTN_ERR_INVALID_ARG;
+    if (!get_encoder()) return ATTN_ERR_CUDA;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    attn_impl::VPrepParams vp{};
+    vp.V = V;
+    vp.V16 = ws + w.v16;
+    vp.partial_max = reinterpret_cast<float*>(ws + w.partial);
+    vp.v_exp = reinterpret_cast<int32_t*>(ws + w.vexp);
+    vp.elems_per_head = static_cast<long long>(N) * d;
+    vp.chunks = w.chunks;
+    vp.heads = B * H_kv;
+
+    CUtensorMap tmQ, tmK, tmV;
+    if (!encode_rows_map(&tmQ, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, N, static_cast<long long>(B) * H) ||
+        !encode_rows_map(&tmK, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, N, static_cast<long long>(B) * H_kv) ||
+        !encode_rows_map(&tmV, vp.V16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, d, N, static_cast<long long>(B) * H_kv))
+        return ATTN_ERR_UNSUPPORTED;
+
+    attn_impl::TcParams p{};
+    p.O = O;
+    p.LSE = LSE;
+    p.kv_len = kv_len;
+    p.v_exp = vp.v_exp;
+    p.B = B; p.H = H; p.H_kv = H_kv; p.N = N; p.group = H / H_kv;
+    p.n_pairs = (N + 255) / 256;
+    p.causal = causal;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.debug_skip_kv_load = g_skip_kv_load.load();
+
+    if (attn_impl::launch_vprep(vp, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
+    const bool timed = ev0 && ev1;
+    if (timed && cudaEventRecord(ev0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (attn_impl::launch_attn_tc(d, out_dtype == ATTN_BF16, tmQ, tmK, tmV, p, stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (timed && cudaEventRecord(ev1, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+attn_status attn_check(cudaStream_t stream) {
+    uint32_t bits = 0;
+    if (attn_impl::read_and_clear_error(&bits, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    return bits ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+const char* attn_status_string(attn_status s) {
+    switch (s) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    }
+    return "ATTN_UNKNOWN_STATUS";
+}
+
+int attn_launches_per_call(attn_dtype in_dtype) { return in_dtype == ATTN_BF16 ? 3 : 1; }
+
+void attn_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs); }
+
+void attn_debug_set_skip_kv_load(int on) { g_skip_kv_load.store(on ? 1 : 0); }
+
+float attn_event_elapsed_ms(cudaEvent_t start, cudaEvent_t stop) {
+    float ms = -1.f;
+    if (!start || !stop || cudaEventElapsedTime(&ms, start, stop) != cudaSuccess) return -1.f;
+    return ms;
+}
+
+void attn_set_kernel_events(cudaEvent_t start, cudaEvent_t stop) {
+    g_ev_start.store(start && stop ? start : nullptr);
+    g_ev_stop.store(start && stop ? stop : nullptr);
+}
+
+}  // extern "C"

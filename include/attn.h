@@ -1,0 +1,130 @@
+/*
+ * attn.h - C ABI of libattn.so: exact multi-head attention forward on NVIDIA B300 (sm_103a).
+ *
+ * The operation (for every batch b, query head h, query row i; kv = h / (H / H_kv)):
+ *
+ *     s_ij  = scale * sum_k Q[b,h,i,k] K[b,kv,j,k]
+ *     valid = j < kv_len[b]  and  (causal == 0  or  j <= i)
+ *     O_i   = sum_{valid j} exp(s_ij - m_i) V[b,kv,j,:] / l_i,   m_i = max_{valid j} s_ij,
+ *             l_i = sum_{valid j} exp(s_ij - m_i)
+ *     LSE_i = m_i + ln l_i        (natural log; a row without valid keys gets O = 0, LSE = -inf)
+ *
+ * This is the attention of the standard_attention listings on the pages "AI训练的最大障碍不是算力,
+ * 而是'内存墙'" (zsdodo.com) and "闪电注意力：革命性地提高Transformer效率" (unite.ai), computed the
+ * tiled way those pages describe: the unite.ai section "闪电注意力的数学原理" (softmax decomposition
+ * and merging of per-block partial results), the running maximum / running sum recurrence of the
+ * safe_softmax_block listing (zsdodo.com) and the unnormalised accumulator with one final division of
+ * section 4.1.3 "算法流程详解" of "第四章 注意力机制实战案例" (aiknowledge.cn). The score matrix never
+ * goes to device memory. Grouped- and multi-query heads (H_kv < H) follow the unite.ai section
+ * "闪电注意力-2"; key padding (kv_len) follows the attention_mask of "动态序列处理" on
+ * "基于AIFI多头注意力机制的高效序列建模实战" (qqiyuan.cn).
+ *
+ * Layouts (all contiguous, row-major, device memory):
+ *   Q   [B, H,    N, d]     K, V [B, H_kv, N, d]     (in_dtype: bf16 or fp32, the same for all three)
+ *   O   [B, H,    N, d]     (out_dtype: fp32, or bf16 for bf16 inputs)
+ *   LSE [B, H,    N]        fp32, may be NULL (not written)
+ *   kv_len int32 [B], may be NULL (= N for every batch); values are clamped to [0, N].
+ *
+ * Precision. fp32 inputs are computed in exact fp32 arithmetic (CUDA cores). bf16 inputs use the
+ * tensor cores: Q K^T is exact bf16 products with fp32 accumulation; the softmax state (m, l) is
+ * fp32 per row; the probabilities enter P V as fp16 and V is converted to fp16 with a per-head
+ * power-of-two scale (exact for bf16 values in fp16 range), accumulating O in fp32.
+ *
+ * Ownership and asynchrony. The caller owns every buffer. The library never allocates device
+ * memory in attn_fwd: bf16 inputs need a caller-provided workspace of attn_workspace_bytes() bytes
+ * (device memory, 256-byte aligned; its contents need no initialisation and are scratch between
+ * calls; two calls that overlap on the GPU must not share it). The call only enqueues work on
+ * `stream` and returns; results are ready when the stream reaches that point. The library keeps
+ * one device error word per device (for bounded-wait timeouts) and no other state.
+ *
+ * Errors. attn_fwd validates its arguments and returns without launching anything on: a NULL
+ * Q/K/V/O pointer, B, H, H_kv or N <= 0, H % H_kv != 0, d not in {64, 128}, scale not finite or
+ * <= 0, a Q/K/V/O/workspace pointer not 16-byte aligned (workspace: 256), too small a workspace,
+ * or an unsupported dtype pair (fp32 inputs with bf16 output) -> ATTN_ERR_INVALID_ARG or
+ * ATTN_ERR_UNSUPPORTED. A failed launch returns ATTN_ERR_CUDA. Every wait inside the tensor-core
+ * kernel gives up after a time limit (about one second) instead of hanging the GPU; it then records
+ * ATTN_ERR_TIMEOUT in the device error word, and attn_check() reports it.
+ */
+#ifndef EXACT_TILED_ATTENTION_B300_ATTN_H
+#define EXACT_TILED_ATTENTION_B300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,
+    ATTN_ERR_UNSUPPORTED = 2,
+    ATTN_ERR_CUDA = 3,
+    ATTN_ERR_TIMEOUT = 4
+} attn_status;
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+/*
+ * Bytes of device workspace attn_fwd needs for these sizes (0 for fp32 inputs). For bf16 inputs it
+ * holds the fp16 copy of V ([B, H_kv, N, d]) plus per-head range data. Returns 0 for invalid sizes.
+ */
+size_t attn_workspace_bytes(int B, int H, int H_kv, int N, int d, attn_dtype in_dtype);
+
+/*
+ * Attention forward (see the top of this file for the operation, layouts, ownership and errors).
+ *   Q, K, V      device pointers, in_dtype
+ *   O            device pointer, out_dtype
+ *   LSE          device fp32 pointer or NULL
+ *   B, H, H_kv, N, d   sizes; d in {64, 128}; H % H_kv == 0
+ *   scale        score scale (typically 1/sqrt(d)); finite and > 0
+ *   causal       0 or 1: mask keys j > i
+ *   kv_len       device int32 [B] or NULL
+ *   workspace    device pointer to attn_workspace_bytes() bytes (may be NULL when that is 0)
+ *   stream       CUDA stream the work is enqueued on (0 = legacy default stream)
+ */
+attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
+                     int N, int d, float scale, int causal, const int32_t* kv_len, attn_dtype in_dtype,
+                     attn_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the calling device's error word. Returns ATTN_OK,
+ * ATTN_ERR_TIMEOUT (a bounded wait inside a kernel ran out; the results of that call are invalid)
+ * or ATTN_ERR_CUDA (the stream reported an error).
+ */
+attn_status attn_check(cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(attn_status s);
+
+/* Number of kernel launches attn_fwd enqueues for these arguments (1 for fp32, 3 for bf16). */
+int attn_launches_per_call(attn_dtype in_dtype);
+
+/*
+ * Test hooks for the failure path (not for production use).
+ * attn_debug_set_wait_limit_ns: time limit of every bounded wait in the tensor-core kernel
+ *   (default 1e9 ns; 0 restores the default).
+ * attn_debug_set_skip_kv_load: when non-zero, the next attn_fwd calls make the TMA producer
+ *   skip issuing the load of key tile 0, so the consumer's wait on it runs out and the kernel
+ *   reports ATTN_ERR_TIMEOUT through attn_check(). Nothing is left in flight.
+ */
+void attn_debug_set_wait_limit_ns(uint64_t ns);
+void attn_debug_set_skip_kv_load(int on);
+
+/*
+ * Timing hook for benchmarks: while set (both non-NULL), every attn_fwd call records `start` on its
+ * stream immediately before the main attention kernel and `stop` immediately after it, so that
+ * cudaEventElapsedTime gives that kernel's duration on the stream it runs on. The events are
+ * created and owned by the caller. attn_set_kernel_events(NULL, NULL) turns the hook off.
+ */
+void attn_set_kernel_events(cudaEvent_t start, cudaEvent_t stop);
+
+/* Milliseconds between two recorded events (cudaEventElapsedTime); -1 on error. */
+float attn_event_elapsed_ms(cudaEvent_t start, cudaEvent_t stop);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_TILED_ATTENTION_B300_ATTN_H */

@@ -1,0 +1,77 @@
+"""The C-ABI library: it loads without a GPU, exports every function include/attn.h declares, and
+rejects invalid arguments on the host before launching anything (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_tiled_attention_50_b300 import build
+    build.build()
+    from exact_tiled_attention_50_b300 import attn
+    return attn
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(attn_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_check", "attn_status_string", "attn_workspace_bytes"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+    assert set(lib.EXPORTED) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    assert lib.status_string(0) == "ATTN_OK"
+    assert lib.status_string(4) == "ATTN_ERR_TIMEOUT"
+    assert lib.status_string(99) == "ATTN_UNKNOWN_STATUS"
+
+
+def test_workspace_bytes(lib):
+    import torch
+    assert lib.workspace_bytes(1, 1, 1, 256, 64, torch.float32) == 0
+    w = lib.workspace_bytes(2, 32, 8, 8192, 128, torch.bfloat16)
+    assert w >= 2 * 8 * 8192 * 128 * 2 and w % 256 == 0
+    assert lib.workspace_bytes(1, 3, 2, 128, 64, torch.bfloat16) == 0  # H % H_kv != 0
+    assert lib.workspace_bytes(1, 1, 1, 128, 96, torch.bfloat16) == 0  # unsupported d
+
+
+def _call(lib, **kw):
+    a = dict(Q=4096, K=4096, V=4096, O=4096, LSE=None, B=1, H=2, H_kv=1, N=128, d=64, scale=0.125, causal=0,
+             kv_len=None, ind=1, outd=0, ws=4096, ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.lib.attn_fwd(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["H_kv"], a["N"], a["d"],
+                            a["scale"], a["causal"], a["kv_len"], a["ind"], a["outd"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(Q=None), dict(K=None), dict(V=None), dict(O=None),
+    dict(B=0), dict(H=0), dict(H_kv=0), dict(N=0), dict(N=-5),
+    dict(H=3, H_kv=2), dict(d=96), dict(d=256), dict(d=0),
+    dict(scale=0.0), dict(scale=-1.0), dict(scale=float("inf")), dict(scale=float("nan")),
+    dict(causal=2), dict(Q=4100), dict(O=4104), dict(ind=7), dict(outd=9),
+    dict(ws=None), dict(ws=4096 + 16), dict(ws_bytes=100),
+])
+def test_invalid_arguments_rejected_without_launch(lib, bad):
+    assert _call(lib, **bad) == lib.ATTN_ERR_INVALID_ARG
+
+
+def test_unsupported_combination(lib):
+    assert _call(lib, ind=0, outd=1) == lib.ATTN_ERR_UNSUPPORTED

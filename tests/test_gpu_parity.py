@@ -1,0 +1,158 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
+
+Small and ragged shapes are compared element by element against the full oracle; the full-size
+workloads (the ones the benchmark times) are compared on sampled rows, each evaluated exactly by the
+row-sampled oracle over all keys.
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_tiled_attention_50_b300 import inputs
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from exact_tiled_attention_50_b300 import attn  # noqa: F401  (fails loudly without libattn.so)
+    assert torch.cuda.is_available()
+    yield
+
+
+# ---------------------------------------------------------------- the five workload families
+def test_tiny_fp32_full():
+    x = inputs.make_inputs(inputs.WORKLOADS["tiny_b1h1_n256_d64_f32"])
+    parity.check_full(x, "f32", what="tiny fp32")
+
+
+def test_b4h8_n1024_d64_full():
+    x = inputs.make_inputs(inputs.WORKLOADS["b4h8_n1024_d64"])
+    parity.check_full(x, "bf16", what="b4h8 n1024 d64")
+
+
+def test_b8h16_n4096_causal_padded_sampled():
+    x = inputs.make_inputs(inputs.WORKLOADS["b8h16_n4096_d128_causal_padded"])
+    parity.check_sampled(x, "bf16", per_head=24, what="b8h16 n4096 causal padded")
+
+
+@pytest.mark.parametrize("name", ["gqa_b2h32kv8_n8192_d128_causal", "mqa_b2h32kv1_n8192_d128_causal"])
+def test_gqa_mqa_n8192_sampled(name):
+    x = inputs.make_inputs(inputs.WORKLOADS[name])
+    parity.check_sampled(x, "bf16", per_head=16, what=name)
+
+
+@pytest.mark.parametrize("n", [512, 1024, 2048, 4096, 8192, 16384])
+@pytest.mark.parametrize("causal", [False, True])
+def test_peaky_sweep_sampled(n, causal):
+    tag = "causal" if causal else "noncausal"
+    x = inputs.make_inputs(inputs.WORKLOADS[f"sweep_b1h16_d128_n{n}_{tag}_peaky"])
+    parity.check_sampled(x, "bf16", per_head=64 if n >= 8192 else 128, what=f"sweep n{n} {tag}")
+
+
+def test_peaky_sweep_n2048_full():
+    x = inputs.make_inputs(inputs.WORKLOADS["sweep_b1h16_d128_n2048_causal_peaky"])
+    parity.check_full(x, "bf16", what="sweep n2048 causal (full)")
+
+
+# ---------------------------------------------------------------- edges: ragged sizes, masks, heads
+@pytest.mark.parametrize("N", [1, 2, 100, 127, 128, 129, 200, 255, 256, 257, 384, 513])
+@pytest.mark.parametrize("d", [64, 128])
+def test_ragged_lengths(N, d):
+    x = inputs.custom(2, 4, 2, N, d, causal=False, seed=N * 7 + d)
+    parity.check_full(x, "bf16", what=f"N={N} d={d}")
+    x = inputs.custom(2, 4, 2, N, d, causal=True, seed=N * 7 + d + 1)
+    parity.check_full(x, "bf16", what=f"N={N} d={d} causal")
+
+
+@pytest.mark.parametrize("H,H_kv", [(8, 8), (8, 2), (8, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_groups(H, H_kv, causal):
+    x = inputs.custom(2, H, H_kv, 300, 128, causal=causal, padded=True, peaky=True, seed=H * 10 + H_kv)
+    parity.check_full(x, "bf16", what=f"H={H} H_kv={H_kv} causal={causal}")
+
+
+@pytest.mark.parametrize("lens", [[1, 1], [299, 300], [300, 300], [0, 171], [129, 128], [256, 1]])
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_padding(lens, causal):
+    x = inputs.custom(2, 2, 1, 300, 64, causal=causal, kv_len=lens, seed=sum(lens))
+    parity.check_full(x, "bf16", what=f"kv_len={lens} causal={causal}")
+
+
+def test_kv_len_out_of_range_is_clamped():
+    x = inputs.custom(2, 2, 2, 200, 64, kv_len=[-5, 10_000], seed=9)
+    O, L = parity.run_gpu(x)
+    import oracle
+    O_ref, L_ref = oracle.attention(x.q, x.k, x.v, x.scale, kv_len=[0, 200])
+    parity.compare(O, L, O_ref, L_ref, "bf16", what="clamped kv_len")
+
+
+@pytest.mark.parametrize("N", [1, 33, 256, 300])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_path(N, causal):
+    for d in (64, 128):
+        x = inputs.custom(2, 4, 2, N, d, dtype="f32", causal=causal, padded=True, seed=N + d)
+        parity.check_full(x, "f32", what=f"fp32 N={N} d={d}")
+
+
+def test_bf16_output():
+    x = inputs.custom(2, 4, 4, 513, 128, causal=True, peaky=True, seed=5)
+    parity.check_full(x, "bf16", out_dtype=torch.bfloat16, what="bf16 out")
+
+
+def test_large_v_values_use_the_per_head_scale():
+    # V beyond the fp16 range (|V| up to ~1e6): the fp16 copy is scaled by a power of two per head
+    x = inputs.custom(1, 2, 2, 256, 64, seed=11)
+    x.v = (x.v.float() * 2.0 ** 18).to(torch.bfloat16)
+    O, L = parity.run_gpu(x)
+    import oracle
+    O_ref, L_ref = oracle.attention(x.q, x.k, x.v, x.scale)
+    rel = (O.double().cpu().numpy() - O_ref) / 2.0 ** 18
+    assert np.abs(rel).max() <= 2e-3 and np.abs(rel).mean() <= 2e-4
+
+
+# ---------------------------------------------------------------- guard bands, determinism
+def test_guard_bands_untouched():
+    from exact_tiled_attention_50_b300 import attn
+    x = inputs.custom(2, 4, 2, 300, 128, causal=True, padded=True, seed=21)
+    B, H, N, d = x.q.shape
+    pad = 4096
+    canary = 1234.5
+    Obuf = torch.full((pad + B * H * N * d + pad,), canary, dtype=torch.float32, device="cuda")
+    Lbuf = torch.full((pad + B * H * N + pad,), canary, dtype=torch.float32, device="cuda")
+    O = Obuf[pad:pad + B * H * N * d].view(B, H, N, d)
+    L = Lbuf[pad:pad + B * H * N].view(B, H, N)
+    attn.attn_fwd(x.q.cuda(), x.k.cuda(), x.v.cuda(), scale=x.scale, causal=True, kv_len=x.kv_len.cuda(),
+                  out=O, lse=L)
+    assert attn.check() == attn.ATTN_OK
+    for buf, n in ((Obuf, B * H * N * d), (Lbuf, B * H * N)):
+        assert bool((buf[:pad] == canary).all()) and bool((buf[pad + n:] == canary).all())
+    import oracle
+    O_ref, L_ref = oracle.attention(x.q, x.k, x.v, x.scale, causal=True, kv_len=x.kv_len)
+    parity.compare(O, L, O_ref, L_ref, "bf16", what="guarded")
+
+
+def test_bitwise_deterministic():
+    x = inputs.custom(1, 8, 2, 1000, 128, causal=True, padded=True, peaky=True, seed=3)
+    O1, L1 = parity.run_gpu(x)
+    O2, L2 = parity.run_gpu(x)
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+
+
+# ---------------------------------------------------------------- failure path (bounded waits)
+def test_bounded_wait_timeout_is_reported_and_context_survives():
+    """The producer skips one load (a barrier that nothing completes); the kernel's bounded wait runs
+    out, it records ATTN_ERR_TIMEOUT and exits; the next call on the same context works."""
+    from exact_tiled_attention_50_b300 import attn
+    x = inputs.custom(1, 1, 1, 256, 64, seed=4)
+    attn.lib.attn_debug_set_wait_limit_ns(50_000_000)
+    attn.lib.attn_debug_set_skip_kv_load(1)
+    try:
+        attn.attn_fwd(x.q.cuda(), x.k.cuda(), x.v.cuda(), scale=x.scale)
+        assert attn.check() == attn.ATTN_ERR_TIMEOUT
+    finally:
+        attn.lib.attn_debug_set_skip_kv_load(0)
+        attn.lib.attn_debug_set_wait_limit_ns(0)
+    assert attn.check() == attn.ATTN_OK  # the error word was cleared
+    parity.check_full(x, "bf16", what="after timeout")
