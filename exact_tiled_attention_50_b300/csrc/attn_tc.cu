@@ -10,20 +10,25 @@
 // (unite.ai). Q-tile-outer / key-tile-inner order as in those listings, so that one CTA owns a row's
 // state for its whole lifetime.
 //
-// Blackwell mapping (one CTA per SM, 320 threads):
+// Blackwell mapping (one CTA per SM, 384 threads = 3 warpgroups):
 //   warps 0-3  softmax warpgroup for query tile 0 (rows 0-127 of the CTA's 256 rows)
 //   warps 4-7  softmax warpgroup for query tile 1 (rows 128-255)
-//   warp  8    tensor-memory owner and MMA issuer (one thread issues every tcgen05.mma)
-//   warp  9    TMA producer (Q tiles once, then a ring of K / V tiles)
+//   warp  8    tensor-memory owner and MMA issuer (converged warp; one elected lane issues)
+//   warp  9    TMA producer (Q_0, Q_1 and K_0 once, then a ring of (V_j, K_j+1) stages)
+//   warps 10-11 idle (they complete the third warpgroup for the register split)
 // Tensor memory (512 columns x 128 lanes x 32 bit): S_0 [0,128), S_1 [128,256), O_0 and O_1 after
 // that (d columns each). P_t (fp16, two per column) overwrites the first 64 columns of S_t after the
 // softmax has read S_t into registers; the P V MMA reads P straight from tensor memory.
-// The MMA thread issues, per key tile j:  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so that while one
-// warpgroup computes exponentials the tensor core works on the other tile (ping-pong).
+// The MMA warp issues, per key tile j:  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so that while one
+// warpgroup computes exponentials the tensor core works on the other tile (ping-pong). S_t(j+1)
+// overwrites the columns PV_t(j) reads P from; it is issued after PV_t(j) by the same thread and
+// relies on the tensor pipe executing MMAs in issue order.
 // The lazy rescale keeps a row's reference maximum until the tile maximum exceeds it by more than
-// 2^8 (log2 domain); exponentials are then at most 256 and the final O / l is unchanged, since O and
-// l use the same reference. V enters the P V product as fp16 (a per-head power-of-two scale keeps
-// it in range); Q K^T is bf16 x bf16 with fp32 accumulation.
+// 2^15 (log2 domain); exponentials are then at most 2^15 (fp16 holds them) and the final O / l is
+// unchanged, since O and l use the same reference. P is handed to the MMA warp in two halves (keys
+// 0-63, 64-127) so that the first four P V k-steps overlap the second half's exponentials.
+// V enters the P V product as fp16 (a per-head power-of-two scale keeps it in range); Q K^T is
+// bf16 x bf16 with fp32 accumulation.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -40,22 +45,51 @@ using namespace attn_sm103;
 
 __device__ unsigned int g_attn_error = 0;
 
+// Optional timeline trace (builds with -DATTN_TRACE only): clock64 stamps of CTA 0's MMA warp and
+// of thread 0 of each softmax warpgroup, per key tile, for profiling the pipeline by hand.
+#ifdef ATTN_TRACE
+constexpr int TRACE_J = 128, TRACE_EV = 8;
+__device__ long long g_attn_trace[3][TRACE_J][TRACE_EV];
+#define ATTN_TRACE_AT(role, j, ev)                                                    \
+    do {                                                                             \
+        if (blockIdx.x == 0 && (j) < TRACE_J) g_attn_trace[role][j][ev] = clock64(); \
+    } while (0)
+#else
+#define ATTN_TRACE_AT(role, j, ev) \
+    do {                           \
+    } while (0)
+#endif
+
 namespace {
 
 constexpr int BLOCK_M = 128;              // query rows per tile (tcgen05 M)
 constexpr int BLOCK_N = 128;              // keys per tile
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;          // 3 warpgroups
 constexpr int MMA_WARP = 8;
 constexpr int TMA_WARP = 9;
-constexpr float RESCALE_THRESHOLD = 8.0f; // log2 units
+// Lazy rescale: a row keeps its reference maximum until a tile's maximum exceeds it by more than
+// 2^15 (log2 units); exponentials then stay <= 2^15, inside the fp16 range of P (65504).
+constexpr float RESCALE_THRESHOLD = 15.0f;
 constexpr uint32_t TMEM_COLS = 512;
+// Register split: the block launches with 384 x 168 = 64512 registers; the two softmax
+// warpgroups raise theirs to 208 and the MMA/TMA warpgroup lowers its to 88:
+// 2*128*208 + 128*88 = 64512 (every sub-partition holds two softmax warps and one other warp:
+// 2*208 + 88 = 504 <= 512 registers per lane).
+constexpr int LAUNCH_REGS = 168;
+constexpr uint32_t SOFTMAX_REGS = 208;
+constexpr uint32_t CONTROL_REGS = 88;
+static_assert(2 * 128 * SOFTMAX_REGS + 128 * CONTROL_REGS <= NUM_THREADS * LAUNCH_REGS, "register split");
 
 template <int D>
 struct Cfg {
     static constexpr int NB = D / 64;                 // 64-element (128-byte) boxes per row
     static constexpr int TILE_BYTES = NB * 16384;     // one 128 x D tile of 16-bit values
-    static constexpr int NS = (D == 128) ? 4 : 8;     // K/V ring stages
-    static constexpr int SMEM_BYTES = 1024 + 2 * TILE_BYTES + NS * TILE_BYTES;
+    // Shared memory: Q_0, Q_1, K_0, then NP ring stages of (V_j, K_j+1), consumed together.
+    static constexpr int NP = (D == 128) ? 2 : 4;
+    static constexpr int OFF_K0 = 2 * TILE_BYTES;
+    static constexpr int OFF_RING = 3 * TILE_BYTES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // V slot then K slot
+    static constexpr int SMEM_BYTES = 1024 + OFF_RING + NP * STAGE_BYTES;
     static constexpr uint32_t IDESC_S = idesc_f16(BLOCK_M, BLOCK_N, 1, 1, 0, 0);  // bf16, K-major both
     static constexpr uint32_t IDESC_O = idesc_f16(BLOCK_M, D, 0, 0, 0, 1);        // f16, B (V) MN-major
     static constexpr uint32_t TMEM_O = 256;
@@ -81,15 +115,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ0 = smem;
-    uint8_t* sKV = smem + 2 * C::TILE_BYTES;
 
-    __shared__ __align__(8) uint64_t bar_q;
-    __shared__ __align__(8) uint64_t bar_kv_full[C::NS];
-    __shared__ __align__(8) uint64_t bar_kv_empty[C::NS];
-    __shared__ __align__(8) uint64_t bar_s_full[2];
-    __shared__ __align__(8) uint64_t bar_p_full[2];
-    __shared__ __align__(8) uint64_t bar_o_full[2];
+    __shared__ __align__(8) uint64_t bar_q;                 // Q_0, Q_1 and K_0 landed
+    __shared__ __align__(8) uint64_t bar_full[C::NP];       // ring stage (V_j, K_j+1) landed
+    __shared__ __align__(8) uint64_t bar_empty[C::NP];      // ring stage free again
+    __shared__ __align__(8) uint64_t bar_s_full[2];         // S_t in TMEM
+    __shared__ __align__(8) uint64_t bar_p_full[2][2];      // half h of P_t in TMEM (O_t rescaled)
+    __shared__ __align__(8) uint64_t bar_o_full[2];         // last P V into O_t done
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
@@ -105,15 +137,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int h = bh - b * p.H;
     const int zkv = b * p.H_kv + h / p.group;
     const int kv_valid = clamp_len(p.kv_len, b, p.N);
-    int q0[2], nkv[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        q0[t] = (2 * pair + t) * BLOCK_M;
-        const bool exists = q0[t] < p.N;
-        const int limit = p.causal ? min(kv_valid, q0[t] + BLOCK_M) : kv_valid;
-        nkv[t] = exists ? (limit + BLOCK_N - 1) / BLOCK_N : 0;
-    }
-    const int nmax = max(nkv[0], nkv[1]);
+    // query tile t covers rows [q0_t, q0_t + 128); it needs key tiles [0, nkv_t)
+    auto tile_nkv = [&](int q0) {
+        const int limit = p.causal ? min(kv_valid, q0 + BLOCK_M) : kv_valid;
+        return q0 < p.N ? (limit + BLOCK_N - 1) / BLOCK_N : 0;
+    };
+    const int q0_0 = 2 * pair * BLOCK_M, q0_1 = q0_0 + BLOCK_M;
+    const int nkv_0 = tile_nkv(q0_0), nkv_1 = tile_nkv(q0_1);
+    const int nmax = max(nkv_0, nkv_1);
 
     // ---- setup ----
     if (warp == MMA_WARP) {
@@ -122,13 +153,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (threadIdx.x == TMA_WARP * 32) {
         mbar_init(&bar_q, 1);
-        for (int s = 0; s < C::NS; ++s) {
-            mbar_init(&bar_kv_full[s], 1);
-            mbar_init(&bar_kv_empty[s], 1);
+        for (int s = 0; s < C::NP; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bar_s_full[t], 1);
-            mbar_init(&bar_p_full[t], 128);
+            mbar_init(&bar_p_full[t][0], 128);
+            mbar_init(&bar_p_full[t][1], 128);
             mbar_init(&bar_o_full[t], 1);
         }
         mbar_init(&bar_drain, 1);
@@ -144,142 +176,168 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = tmem_base_sh;
     const uint64_t limit_ns = p.wait_limit_ns;
 
-    if (warp == TMA_WARP) {
-        // ================================ TMA producer ================================
-        if (lane == 0 && nmax > 0) {
-            const uint64_t pol_kv = l2_policy_evict_last();
-            const uint64_t pol_q = l2_policy_evict_first();
-            uint32_t qbytes = 0;
-            for (int t = 0; t < 2; ++t) qbytes += nkv[t] > 0 ? C::TILE_BYTES : 0;
-            mbar_arrive_expect_tx(&bar_q, qbytes);
-            for (int t = 0; t < 2; ++t)
-                if (nkv[t] > 0)
+    // Each role's code sits inside the branch that set its register budget, so that the register
+    // allocator sees the larger budget only where it holds.
+    if (warp >= 8) {
+        regs_decrease<CONTROL_REGS>();
+        if (warp == TMA_WARP && nmax > 0) {
+            // ============================== TMA producer (one lane) ==============================
+            if (elect_one()) {
+                const uint64_t pol_kv = l2_policy_evict_last();
+                const uint64_t pol_q = l2_policy_evict_first();
+                uint32_t qbytes = C::TILE_BYTES;  // K_0
+                qbytes += nkv_0 > 0 ? C::TILE_BYTES : 0;
+                qbytes += nkv_1 > 0 ? C::TILE_BYTES : 0;
+                mbar_arrive_expect_tx(&bar_q, qbytes);
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+                    if ((t ? nkv_1 : nkv_0) > 0)
+                        for (int bx = 0; bx < C::NB; ++bx)
+                            tma_load_3d_hint(smem + t * C::TILE_BYTES + bx * 16384, &tmQ, &bar_q, bx * 64,
+                                             t ? q0_1 : q0_0, bh, pol_q);
+                if (!p.debug_skip_kv_load)  // failure-path test: K_0 is never loaded
                     for (int bx = 0; bx < C::NB; ++bx)
-                        tma_load_3d_hint(sQ0 + t * C::TILE_BYTES + bx * 16384, &tmQ, &bar_q, bx * 64, q0[t], bh,
-                                         pol_q);
-            int it_done = 0;
-            bool ok = true;
-            for (int it = 0; it < 2 * nmax; ++it) {
-                const int stage = it % C::NS;
-                if (it >= C::NS) {
-                    if (!mbar_wait(&bar_kv_empty[stage], ((it / C::NS) - 1) & 1, limit_ns, &abort_flag)) {
+                        tma_load_3d_hint(smem + C::OFF_K0 + bx * 16384, &tmK, &bar_q, bx * 64, 0, zkv, pol_kv);
+                int issued = 0;
+                bool ok = true;
+                for (int j = 0; j < nmax; ++j) {
+                    const int st = j % C::NP;
+                    if (j >= C::NP &&
+                        !mbar_wait(&bar_empty[st], ((j / C::NP) - 1) & 1, limit_ns, &abort_flag)) {
                         record_failure(&abort_flag, ERRBIT_WAIT_EMPTY);
                         ok = false;
                         break;
                     }
+                    const bool has_k = j + 1 < nmax;
+                    mbar_arrive_expect_tx(&bar_full[st], has_k ? 2 * C::TILE_BYTES : C::TILE_BYTES);
+                    uint8_t* dst = smem + C::OFF_RING + st * C::STAGE_BYTES;
+                    for (int bx = 0; bx < C::NB; ++bx)
+                        tma_load_3d_hint(dst + bx * 16384, &tmV, &bar_full[st], bx * 64, j * BLOCK_N, zkv, pol_kv);
+                    if (has_k)
+                        for (int bx = 0; bx < C::NB; ++bx)
+                            tma_load_3d_hint(dst + C::TILE_BYTES + bx * 16384, &tmK, &bar_full[st], bx * 64,
+                                             (j + 1) * BLOCK_N, zkv, pol_kv);
+                    issued = j + 1;
                 }
-                const int j = it >> 1;
-                const bool is_v = it & 1;
-                if (!is_v && j == 0 && p.debug_skip_kv_load) {
-                    it_done = it + 1;
-                    continue;  // failure-path test: this tile is never loaded
-                }
-                mbar_arrive_expect_tx(&bar_kv_full[stage], C::TILE_BYTES);
-                uint8_t* dst = sKV + stage * C::TILE_BYTES;
-                for (int bx = 0; bx < C::NB; ++bx)
-                    tma_load_3d_hint(dst + bx * 16384, is_v ? &tmV : &tmK, &bar_kv_full[stage], bx * 64,
-                                     j * BLOCK_N, zkv, pol_kv);
-                it_done = it + 1;
-            }
-            // On failure, wait (bounded) for the copies this thread issued and nobody consumed, so
-            // that no TMA write lands in shared memory after the CTA has exited.
-            if (!ok || abort_flag) {
-                volatile int never = 0;  // these waits must not be cut short by the abort flag
-                (void)mbar_wait(&bar_q, 0, limit_ns, &never);
-                const int first = it_done > C::NS ? it_done - C::NS : 0;
-                for (int it = first; it < it_done; ++it) {
-                    if (it == 0 && p.debug_skip_kv_load) continue;
-                    (void)mbar_wait(&bar_kv_full[it % C::NS], (it / C::NS) & 1, limit_ns, &never);
+                // On failure, wait (bounded) for the copies this thread issued, so that no TMA write
+                // lands in shared memory after the CTA has exited.
+                if (!ok || abort_flag) {
+                    volatile int never = 0;  // these waits must not be cut short by the abort flag
+                    if (!p.debug_skip_kv_load) (void)mbar_wait(&bar_q, 0, limit_ns, &never);
+                    for (int j = issued > C::NP ? issued - C::NP : 0; j < issued; ++j)
+                        (void)mbar_wait(&bar_full[j % C::NP], (j / C::NP) & 1, limit_ns, &never);
                 }
             }
-        }
-        __syncwarp();
-    } else if (warp == MMA_WARP) {
-        // ================================ MMA issuer ================================
-        if (lane == 0 && nmax > 0) {
-            bool ok = mbar_wait(&bar_q, 0, limit_ns, &abort_flag);
-            if (!ok) record_failure(&abort_flag, ERRBIT_WAIT_Q);
-            const uint32_t sQa = smem_u32(sQ0);
-            const uint32_t sKVa = smem_u32(sKV);
-            auto issue_S = [&](int t, int stage) {
-                const uint32_t qa = sQa + t * C::TILE_BYTES;
-                const uint32_t ka = sKVa + stage * C::TILE_BYTES;
+            __syncwarp();
+        } else if (warp == MMA_WARP && nmax > 0) {
+            // ======================= MMA issuer (converged warp, one lane issues) =======================
+            auto wait_all = [&](uint64_t* bar, uint32_t parity, uint32_t bit) {
+                const bool got = mbar_wait(bar, parity, limit_ns, &abort_flag);
+                if (__all_sync(0xffffffffu, got)) return true;
+                if (!got) record_failure(&abort_flag, bit);
+                return false;
+            };
+            // Descriptors are built once; a k-step or stage moves the start address, which is the
+            // low field (address >> 4) of the descriptor, so offsets are added to it directly.
+            const uint64_t dQ = sdesc_sw128(smem_u32(smem), 16, 1024);
+            const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::OFF_K0), 16, 1024);
+            const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING + C::TILE_BYTES), 16, 1024);
+            const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16384, 1024);
+            auto issue_S = [&](int t, uint64_t dk) {
+                const uint64_t a = dQ + static_cast<uint64_t>((t * C::TILE_BYTES) >> 4);
+                const uint32_t d = tmem + t * BLOCK_N;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_ss(tmem + t * BLOCK_N, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                            C::IDESC_S, kk > 0);
+                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                    umma_ss(d, a + off, dk + off, C::IDESC_S, kk > 0);
                 }
             };
-            auto issue_PV = [&](int t, int stage, bool accumulate) {
-                const uint32_t va = sKVa + stage * C::TILE_BYTES;
+            // P V over keys [64*half, 64*half + 64): four k-steps of 16 keys
+            auto issue_PV_half = [&](int t, uint64_t dv, int half, bool accumulate) {
+                const uint32_t d = tmem + C::TMEM_O + t * D;
+                const uint32_t a = tmem + t * BLOCK_N;
 #pragma unroll
-                for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-                    umma_ts(tmem + C::TMEM_O + t * D, tmem + t * BLOCK_N + kk * 8,
-                            sdesc_sw128(va + kk * 2048, 16384, 1024), C::IDESC_O, (accumulate || kk > 0));
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const int kk = half * 4 + k4;
+                    umma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_O,
+                            (accumulate || kk > 0));
+                }
             };
+            bool ok = wait_all(&bar_q, 0, ERRBIT_WAIT_Q);
             if (ok) {
                 tc_fence_after();
-                // prologue: S_t(0) for both tiles from K_0 (ring position 0)
-                ok = mbar_wait(&bar_kv_full[0], 0, limit_ns, &abort_flag);
-                if (!ok) record_failure(&abort_flag, ERRBIT_WAIT_KV);
+                if (elect_one()) {
+                    if (nkv_0 > 0) {
+                        issue_S(0, dK0);
+                        umma_commit(&bar_s_full[0]);
+                    }
+                    if (nkv_1 > 0) {
+                        issue_S(1, dK0);
+                        umma_commit(&bar_s_full[1]);
+                    }
+                }
+                __syncwarp();
             }
-            if (ok) {
+            for (int j = 0; j < nmax && ok; ++j) {
+                const int st = j % C::NP;
+                ATTN_TRACE_AT(0, j, 4);
+                if (!wait_all(&bar_full[st], (j / C::NP) & 1, ERRBIT_WAIT_KV)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                for (int t = 0; t < 2; ++t)
-                    if (nkv[t] > 0) {
-                        issue_S(t, 0);
-                        umma_commit(&bar_s_full[t]);
-                    }
-                umma_commit(&bar_kv_empty[0]);
-                for (int j = 0; j < nmax && ok; ++j) {
-                    const int itV = 2 * j + 1, itK = 2 * j + 2;
-                    const int sV = itV % C::NS, sK = itK % C::NS;
-                    const bool has_next = j + 1 < nmax;
-                    if (!mbar_wait(&bar_kv_full[sV], (itV / C::NS) & 1, limit_ns, &abort_flag)) {
-                        record_failure(&abort_flag, ERRBIT_WAIT_KV);
+                ATTN_TRACE_AT(0, j, 5);
+                const uint64_t dv = dRingV + static_cast<uint64_t>((st * C::STAGE_BYTES) >> 4);
+                const uint64_t dk = dRingK + static_cast<uint64_t>((st * C::STAGE_BYTES) >> 4);
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int n_t = t ? nkv_1 : nkv_0;
+                    if (!ok || j >= n_t) continue;
+                    if (!wait_all(&bar_p_full[t][0], j & 1, ERRBIT_WAIT_P)) {
                         ok = false;
-                        break;
-                    }
-                    if (has_next && !mbar_wait(&bar_kv_full[sK], (itK / C::NS) & 1, limit_ns, &abort_flag)) {
-                        record_failure(&abort_flag, ERRBIT_WAIT_KV);
-                        ok = false;
-                        break;
+                        continue;
                     }
                     tc_fence_after();
-                    for (int t = 0; t < 2; ++t) {
-                        if (j >= nkv[t]) continue;
-                        if (!mbar_wait(&bar_p_full[t], j & 1, limit_ns, &abort_flag)) {
-                            record_failure(&abort_flag, ERRBIT_WAIT_P);
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_PV(t, sV, j > 0);
-                        if (j + 1 < nkv[t]) {
-                            issue_S(t, sK);
+                    ATTN_TRACE_AT(0, j, 2 * t);
+                    if (elect_one()) issue_PV_half(t, dv, 0, j > 0);
+                    __syncwarp();
+                    if (!wait_all(&bar_p_full[t][1], j & 1, ERRBIT_WAIT_P)) {
+                        ok = false;
+                        continue;
+                    }
+                    tc_fence_after();
+                    if (elect_one()) {
+                        issue_PV_half(t, dv, 1, true);
+                        if (j + 1 < n_t) {
+                            issue_S(t, dk);
                             umma_commit(&bar_s_full[t]);
                         } else {
                             umma_commit(&bar_o_full[t]);
                         }
                     }
-                    if (!ok) break;
-                    umma_commit(&bar_kv_empty[sV]);
-                    if (has_next) umma_commit(&bar_kv_empty[sK]);
+                    __syncwarp();
+                    ATTN_TRACE_AT(0, j, 2 * t + 1);
                 }
+                if (!ok) break;
+                if (elect_one()) umma_commit(&bar_empty[st]);
+                __syncwarp();
             }
-            // Drain: every MMA this thread issued has completed before tensor memory is freed.
-            umma_commit(&bar_drain);
+            // Drain: every MMA this warp issued has completed before tensor memory is freed.
+            if (elect_one()) umma_commit(&bar_drain);
+            __syncwarp();
             volatile int never = 0;  // not cut short by the abort flag: the drain must finish
-            if (!mbar_wait(&bar_drain, 0, limit_ns, &never)) record_failure(&abort_flag, ERRBIT_WAIT_DRAIN);
+            const bool drained = mbar_wait(&bar_drain, 0, limit_ns, &never);
+            if (!__all_sync(0xffffffffu, drained) && lane == 0) record_failure(&abort_flag, ERRBIT_WAIT_DRAIN);
         }
-        __syncwarp();
     } else {
+        regs_increase<SOFTMAX_REGS>();
         // ============================ softmax warpgroups ============================
         const int t = warp >> 2;            // query tile of this warpgroup
         const int wq = warp & 3;            // TMEM lane quarter
         const int r = wq * 32 + lane;       // row within the tile
-        const int row = q0[t] + r;          // query index
+        const int q0t = t ? q0_1 : q0_0;
+        const int nkvt = t ? nkv_1 : nkv_0;
+        const int row = q0t + r;            // query index
         const uint32_t lane_off = tmem_lane_base(wq);
         const uint32_t tS = tmem + lane_off + t * BLOCK_N;
         const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
@@ -288,10 +346,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float l_run = 0.f;                  // running sum of exp2(s*sl - m_run)
         bool ok = true;
         const int row_lim = p.causal ? min(kv_valid, row + 1) : kv_valid;  // keys < row_lim are valid
+        const bool trace_me = (threadIdx.x & 127) == 0;
 
-        for (int j = 0; j < nkv[t]; ++j) {
+        for (int j = 0; j < nkvt; ++j) {
             // tcgen05.ld/st below are warp-collective: the warp proceeds only if every lane's wait
             // succeeded
+            if (trace_me) ATTN_TRACE_AT(1 + t, j, 0);
             const bool got = mbar_wait(&bar_s_full[t], j & 1, limit_ns, &abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
                 if (!got) record_failure(&abort_flag, ERRBIT_WAIT_S);
@@ -299,6 +359,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             tc_fence_after();
+            if (trace_me) ATTN_TRACE_AT(1 + t, j, 1);
             uint32_t ra[32], rb[32], rc[32], rd[32];
             tmem_ld32(tS + 0, ra);
             tmem_ld32(tS + 32, rb);
@@ -308,6 +369,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_wait_ld(rb);
             tmem_wait_ld(rc);
             tmem_wait_ld(rd);
+            if (trace_me) ATTN_TRACE_AT(1 + t, j, 2);
             float x[128];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -317,21 +379,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 x[96 + i] = __uint_as_float(rd[i]);
             }
             const int k0 = j * BLOCK_N;
-            if (k0 + BLOCK_N > kv_valid || (p.causal && k0 + BLOCK_N - 1 > q0[t])) {
+            if (k0 + BLOCK_N > kv_valid || (p.causal && k0 + BLOCK_N - 1 > q0t)) {
                 const int lim = row_lim - k0;
 #pragma unroll
                 for (int i = 0; i < 128; ++i)
                     if (i >= lim) x[i] = -INFINITY;
             }
+            // row maximum: four independent chains of three-input maxima
             float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-            for (int i = 4; i < 128; i += 4) {
-                mx0 = fmaxf(mx0, x[i]);
-                mx1 = fmaxf(mx1, x[i + 1]);
-                mx2 = fmaxf(mx2, x[i + 2]);
-                mx3 = fmaxf(mx3, x[i + 3]);
+            for (int i = 4; i < 128; i += 8) {
+                mx0 = max3f(mx0, x[i], x[i + 1]);
+                mx1 = max3f(mx1, x[i + 2], x[i + 3]);
+                mx2 = max3f(mx2, x[i + 4], x[i + 5]);
+                mx3 = max3f(mx3, x[i + 6], x[i + 7]);
             }
-            const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl;
+            const float m_tile = max3f(mx0, mx1, fmaxf(mx2, mx3)) * sl;
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -342,41 +405,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 m_run = m_tile;
                 rescale = true;
             }
+            // Lazy rescale of O_t before any of this tile's P V lands in it (the previous P V into
+            // O_t has completed: its completion preceded the S_t commit this warpgroup waited on).
             if (__any_sync(0xffffffffu, rescale)) {
+                const f32x2 al2 = make_f32x2(alpha, alpha);
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
                     tmem_ld32(tO + c * 32, o);
                     tmem_wait_ld(o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    for (int i = 0; i < 16; ++i) {
+                        float a0, a1;
+                        split_f32x2(mul_f32x2(make_f32x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                                              al2),
+                                    a0, a1);
+                        o[2 * i] = __float_as_uint(a0);
+                        o[2 * i + 1] = __float_as_uint(a1);
+                    }
                     tmem_st32(tO + c * 32, o);
                 }
             }
+            if (trace_me) ATTN_TRACE_AT(1 + t, j, 3);
             const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
-            uint32_t pk0[32], pk1[32];
-            float ls0 = 0.f, ls1 = 0.f;
+            // P = exp2(s * scale*log2e - m), written to TMEM as fp16 pairs over the first 64 columns
+            // of S_t, one half (64 keys) at a time; each half is announced as soon as it is stored.
+            // The scale-and-subtract and the row sum use two-wide fp32 instructions.
+            {
+                const f32x2 sl2 = make_f32x2(sl, sl);
+                const f32x2 nm2 = make_f32x2(-m_sub, -m_sub);
+                f32x2 acc0 = make_f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float a0 = ex2_approx(fmaf(x[2 * i], sl, -m_sub));
-                const float a1 = ex2_approx(fmaf(x[2 * i + 1], sl, -m_sub));
-                const float b0 = ex2_approx(fmaf(x[64 + 2 * i], sl, -m_sub));
-                const float b1 = ex2_approx(fmaf(x[64 + 2 * i + 1], sl, -m_sub));
-                ls0 += a0 + a1;
-                ls1 += b0 + b1;
-                pk0[i] = pack_f16x2(a0, a1);
-                pk1[i] = pack_f16x2(b0, b1);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float e0, e1;
+                        split_f32x2(fma_f32x2(make_f32x2(x[64 * half + 2 * i], x[64 * half + 2 * i + 1]), sl2, nm2),
+                                    e0, e1);
+                        e0 = ex2_approx(e0);
+                        e1 = ex2_approx(e1);
+                        const f32x2 e = make_f32x2(e0, e1);
+                        if (i & 1) acc1 = add_f32x2(acc1, e);
+                        else acc0 = add_f32x2(acc0, e);
+                        pk[i] = pack_f16x2(e0, e1);
+                    }
+                    tmem_st32(tS + 32 * half, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bar_p_full[t][half]);
+                    if (trace_me) ATTN_TRACE_AT(1 + t, j, 4 + half);
+                }
+                float s0, s1, s2, s3;
+                split_f32x2(acc0, s0, s1);
+                split_f32x2(acc1, s2, s3);
+                l_run += (s0 + s1) + (s2 + s3);
             }
-            l_run += ls0 + ls1;
-            tmem_st32(tS + 0, pk0);
-            tmem_st32(tS + 32, pk1);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bar_p_full[t]);
+            if (trace_me) ATTN_TRACE_AT(1 + t, j, 6);
         }
 
         // ---- epilogue: O / l (times the fp16 scale of V), LSE ----
-        if (ok && nkv[t] > 0) {
+        if (ok && nkvt > 0) {
             const bool got = mbar_wait(&bar_o_full[t], 0, limit_ns, &abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
                 if (!got) record_failure(&abort_flag, ERRBIT_WAIT_O);
@@ -384,8 +473,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
         }
-        if (q0[t] < p.N) {
-            const bool have = ok && nkv[t] > 0;
+        if (q0t < p.N) {
+            const bool have = ok && nkvt > 0;
             const float vscale = have ? ldexpf(1.0f, __ldg(p.v_exp + zkv)) : 0.f;
             const float inv = (have && l_run > 0.f) ? vscale / l_run : 0.f;
             const bool store = row < p.N;
@@ -525,6 +614,12 @@ static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, c
     auto kern = attn_fwd_tc_kernel<D, OUT_BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // The register split inside the kernel assumes exactly LAUNCH_REGS registers per thread at
+    // launch; with fewer, the softmax warpgroups' increase could never be granted.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidKernelImage;
     const long long grid = static_cast<long long>(p.n_pairs) * p.B * p.H;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
@@ -539,6 +634,13 @@ cudaError_t launch_attn_tc(int d, bool out_bf16, const CUtensorMap& tmQ, const C
                                  : launch_tc_t<64, false>(tmQ, tmK, tmV16, p, stream);
     return cudaErrorInvalidValue;
 }
+
+#ifdef ATTN_TRACE
+extern "C" int attn_debug_read_trace(long long* host, int n) {
+    if (n < 3 * TRACE_J * TRACE_EV) return -1;
+    return cudaMemcpyFromSymbol(host, g_attn_trace, sizeof(g_attn_trace)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 cudaError_t read_and_clear_error(uint32_t* out, cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);

@@ -23,7 +23,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
+// One lane of the (converged) warp returns true.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e != 0;
+}
 
 // ---------------------------------------------------------------------------------------------
 // mbarrier
@@ -58,17 +67,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase of `bar` with parity `parity` has completed. Returns false if it did not
-// complete within `limit_ns` nanoseconds or if `*abort` became non-zero meanwhile (another role
-// of the CTA gave up); the caller then records the failure and leaves its loop.
+// complete within the limit or if `*abort` became non-zero meanwhile (another role of the CTA gave
+// up); the caller then records the failure and leaves its loop. The limit is counted in SM clock
+// cycles (the cheap per-SM counter; 2 cycles per nanosecond, i.e. `limit_ns` at 2 GHz and longer
+// at lower clocks) and checked only every 64 unsuccessful polls, so that a completed phase is seen
+// without delay.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                           const volatile int* abort) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
+    const long long t0 = clock64();
+    const long long limit_cycles = static_cast<long long>(limit_ns) * 2;
     while (true) {
-        if (mbar_try_wait(a, parity)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(a, parity)) return true;
         if (*abort) return false;
-        if (global_timer_ns() - t0 > limit_ns) return false;
+        if (clock64() - t0 > limit_cycles) return false;
     }
 }
 
@@ -243,6 +258,19 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ uint32_t tmem_lane_base(uint32_t warp_id) { return (32u * (warp_id & 3u)) << 16; }
 
 // ---------------------------------------------------------------------------------------------
+// Per-warpgroup register budget (all four warps of a warpgroup must execute the same one).
+// The increase waits until the block's pool (threads x registers at launch) has room.
+// ---------------------------------------------------------------------------------------------
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------------------------
 // Misc
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
@@ -253,6 +281,41 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// max of three fp32 values (one instruction on sm_100 and later)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Packed pair of fp32 values for the two-wide fp32 instructions of sm_100 and later.
+struct f32x2 {
+    uint64_t v;
+};
+__device__ __forceinline__ f32x2 make_f32x2(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void split_f32x2(f32x2 x, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x.v));
+}
+__device__ __forceinline__ f32x2 fma_f32x2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return r;
+}
+__device__ __forceinline__ f32x2 mul_f32x2(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ f32x2 add_f32x2(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
