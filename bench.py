@@ -17,6 +17,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -33,6 +34,10 @@ from exact_tiled_attention_50_b300 import inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s and % of B300 dense-BF16 peak at N=8192, d=128"
 UNIT = "TFLOP/s"
+# query rows of the fp64 oracle: the CPU-baseline leg times CPU_ROWS rows (10-30 s on the host cores);
+# the reference arm spreads about REF_BUDGET_ROWS rows over all of its steps
+CPU_ROWS = 32768
+REF_BUDGET_ROWS = 262144
 
 
 def load_peaks():
@@ -113,6 +118,36 @@ def flops_of(w) -> float:
     return w.nominal_flops()
 
 
+KERNEL_SOURCES = ("exact_tiled_attention_50_b300/csrc/attn_tc.cu", "exact_tiled_attention_50_b300/csrc/sm103_ptx.cuh",
+                  "exact_tiled_attention_50_b300/csrc/attn_internal.h")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(w):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary of this workload,
+    or None when there is none or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_tc_kernel_b{w.B}h{w.H}_n{w.N}_d{w.d}.md")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            m = re.match(r"^(traffic_bytes_per_launch|kernel_source_sha256_16):\s*(\S+)", line)
+            if m:
+                kv[m.group(1)] = m.group(2)
+    if kv.get("kernel_source_sha256_16") != kernel_source_hash() or "traffic_bytes_per_launch" not in kv:
+        return None
+    return float(kv["traffic_bytes_per_launch"])
+
+
 def oracle_sample_rows(w, n_rows, seed=0):
     rng = np.random.default_rng(seed)
     total = w.B * w.H * w.N
@@ -142,14 +177,16 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     x = inputs.make_inputs(w)
-    r = time_oracle(x, w, args.ref_rows, args.steps, args.warmup)
+    # about REF_BUDGET_ROWS rows over the whole run (a few minutes on 8-16 host cores)
+    rows = max(16, min(args.ref_rows, REF_BUDGET_ROWS // (args.steps + args.warmup)))
+    r = time_oracle(x, w, rows, args.steps, args.warmup)
     line = {
         "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["sec_per_step"] * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, on the host)",
         "impl": "reference",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d, "causal": w.causal,
-                   "sample_rows_per_step": args.ref_rows},
+                   "sample_rows_per_step": rows},
         "cpu_baseline": {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                          "sample": r["sample"]},
         "e2e": {"value": r["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -269,7 +306,8 @@ def run_ours(args, w):
                    "parallelism": f"replicas x{ws} (independent problems per GPU)",
                    "pct_of_peak_bf16": 100.0 * flops / (step_ms * 1e-3) / 1e12 / peaks["bf16"]},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": UNIT,
-                     "frac": achieved / peaks["bf16"], "traffic": args.traffic,
+                     "frac": achieved / peaks["bf16"],
+                     "traffic": args.traffic if args.traffic is not None else profiled_traffic(w),
                      "kernel": "attn_fwd_tc_kernel<128,false>", "kernel_ms": kern_ms,
                      "peak_source": f"{peaks['source']} bf16 burst (cuBLAS); "
                                     f"frac of sustained {achieved / peaks['bf16_sustained']:.3f}"},
@@ -280,7 +318,7 @@ def run_ours(args, w):
         "wall_s_timed_region": wall,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        r = time_oracle(x, w, args.ref_rows, 1, 0)
+        r = time_oracle(x, w, args.cpu_rows, 1, 0)
         line["cpu_baseline"] = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                                 "sample": r["sample"]}
     if rank == 0:
@@ -297,7 +335,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
-    ap.add_argument("--ref-rows", type=int, default=1024, help="oracle query rows per step (reference / cpu leg)")
+    ap.add_argument("--ref-rows", type=int, default=4096, help="max oracle query rows per step (reference arm)")
+    ap.add_argument("--cpu-rows", type=int, default=CPU_ROWS, help="oracle query rows of the cpu_baseline leg")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--traffic", type=float, default=None, help="DRAM bytes per launch from an ncu capture")
     ap.add_argument("--no-cpu-baseline", action="store_true")
