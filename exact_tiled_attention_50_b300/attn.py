@@ -19,7 +19,7 @@ ATTN_F32, ATTN_BF16 = 0, 1
 
 EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_workspace_bytes", "attn_launches_per_call",
             "attn_debug_set_wait_limit_ns", "attn_debug_set_skip_kv_load", "attn_set_kernel_events",
-            "attn_event_elapsed_ms")
+            "attn_event_elapsed_ms", "attn_fwd_noalloc")
 
 
 class AttnError(RuntimeError):
@@ -36,6 +36,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci, ci, vp, sz, vp]
     lib.attn_fwd.restype = ci
+    lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci, ci, vp]
+    lib.attn_fwd_noalloc.restype = ci
     lib.attn_check.argtypes = [vp]
     lib.attn_check.restype = ci
     lib.attn_status_string.argtypes = [ci]
@@ -125,6 +127,25 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return out, lse
+
+
+def attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor],
+                     *, scale: Optional[float] = None, causal: bool = False,
+                     kv_len: Optional[torch.Tensor] = None) -> None:
+    """attn_fwd through the entry point that allocates nothing: the library's fixed device scratch
+    replaces the workspace. q, k, v, out, lse (and kv_len) must already be contiguous CUDA tensors of
+    the shapes attn_fwd takes; this wrapper creates no tensor either."""
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib.attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr() if lse is not None else None, B, H, H_kv, N, d, float(scale),
+                              int(bool(causal)), kv_len.data_ptr() if kv_len is not None else None,
+                              _dtype_code(q.dtype), _dtype_code(out.dtype), stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_noalloc")
 
 
 def check(stream: Optional[torch.cuda.Stream] = None) -> int:

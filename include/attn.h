@@ -123,6 +123,34 @@ void attn_set_kernel_events(cudaEvent_t start, cudaEvent_t stop);
 /* Milliseconds between two recorded events (cudaEventElapsedTime); -1 on error. */
 float attn_event_elapsed_ms(cudaEvent_t start, cudaEvent_t stop);
 
+/*
+ * Attention forward without any device allocation, for callers that cannot allocate device memory
+ * where they run attention (inside a host callback or an allocator's own hooks, under a memory pool
+ * that is fixed at start-up and fully handed out, or in plug-in hosts that forbid device allocation
+ * after initialisation). The method itself has no counterpart on the pages: it is attn_fwd with its
+ * scratch taken from one fixed array instead of a caller workspace.
+ *
+ * Arguments, layouts, results and errors are those of attn_fwd, without workspace/workspace_bytes.
+ * The caller still allocates Q, K, V, O, LSE and kv_len. The scratch is a static device array of
+ * ATTN_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library, which every GPU that loads the library
+ * holds until the process exits. Sizes whose workspace (attn_workspace_bytes) exceeds it return
+ * ATTN_ERR_UNSUPPORTED without launching; use attn_fwd with a workspace for those.
+ *
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture. No call allocates device
+ * memory (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * Every call on a device uses the same array, and the array keeps the contents of the last call.
+ * Nothing in it needs clearing: each call writes every scratch byte it reads before reading it. Two
+ * calls whose work overlaps on the GPU (different streams without ordering, or different host
+ * threads) race on the array and give wrong results; order them on one stream or with events.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+attn_status attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                             int H_kv, int N, int d, float scale, int causal, const int32_t* kv_len,
+                             attn_dtype in_dtype, attn_dtype out_dtype, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
