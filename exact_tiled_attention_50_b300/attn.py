@@ -19,7 +19,8 @@ ATTN_F32, ATTN_BF16 = 0, 1
 
 EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_workspace_bytes", "attn_launches_per_call",
             "attn_debug_set_wait_limit_ns", "attn_debug_set_skip_kv_load", "attn_set_kernel_events",
-            "attn_event_elapsed_ms", "attn_fwd_noalloc")
+            "attn_event_elapsed_ms", "attn_fwd_noalloc", "attn_debug_schedule",
+            "attn_debug_last_error_bits")
 
 
 class AttnError(RuntimeError):
@@ -52,6 +53,10 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_debug_set_skip_kv_load.restype = None
     lib.attn_set_kernel_events.argtypes = [vp, vp]
     lib.attn_set_kernel_events.restype = None
+    lib.attn_debug_last_error_bits.argtypes = []
+    lib.attn_debug_last_error_bits.restype = ctypes.c_uint32
+    lib.attn_debug_schedule.argtypes = [ci, ci, ci, ci, vp, ci, vp, ci]
+    lib.attn_debug_schedule.restype = ci
     lib.attn_event_elapsed_ms.argtypes = [vp, vp]
     lib.attn_event_elapsed_ms.restype = ctypes.c_float
     return lib
@@ -146,6 +151,20 @@ def attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
                               _dtype_code(q.dtype), _dtype_code(out.dtype), stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_noalloc")
+
+
+def schedule(B: int, H: int, N: int, causal: bool, kv_len=None, sms: int = 148):
+    """The persistent kernel's work schedule for these sizes (host computation, no GPU): a list of
+    (cta, b, h, pair, k0, k1, cost, kind) tuples in each CTA's run order."""
+    import numpy as np
+    kv = None if kv_len is None else np.ascontiguousarray(np.asarray(kv_len, dtype=np.int32).reshape(B))
+    kv_ptr = kv.ctypes.data if kv is not None else None
+    n = lib.attn_debug_schedule(B, H, N, int(bool(causal)), kv_ptr, sms, None, 0)
+    if n < 0:
+        raise ValueError("invalid schedule arguments")
+    out = np.zeros((max(n, 1), 8), dtype=np.int32)
+    lib.attn_debug_schedule(B, H, N, int(bool(causal)), kv_ptr, sms, out.ctypes.data, n)
+    return [tuple(int(v) for v in row) for row in out[:n]]
 
 
 def check(stream: Optional[torch.cuda.Stream] = None) -> int:

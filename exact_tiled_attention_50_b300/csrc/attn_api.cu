@@ -8,6 +8,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "../../include/attn.h"
 #include "attn_internal.h"
@@ -17,6 +18,7 @@ namespace {
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;  // 1 s
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int> g_skip_kv_load{0};
+std::atomic<uint32_t> g_last_error_bits{0};
 std::atomic<cudaEvent_t> g_ev_start{nullptr};
 std::atomic<cudaEvent_t> g_ev_stop{nullptr};
 
@@ -37,8 +39,10 @@ bool get_encoder() {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Workspace: fp16 copy of V | per-chunk |V| maxima | per-head exponents | schedule batch offsets |
+// partial-result flags | partial results of split work units (each piece 256 B aligned).
 struct WorkspaceLayout {
-    size_t v16 = 0, partial = 0, vexp = 0, total = 0;
+    size_t v16 = 0, partial = 0, vexp = 0, boff = 0, flags = 0, part = 0, total = 0;
     int chunks = 0;
 };
 
@@ -49,8 +53,26 @@ bool workspace_layout(int B, int H_kv, int N, int d, WorkspaceLayout* w) {
     w->v16 = 0;
     w->partial = round_up(static_cast<size_t>(heads * elems_per_head) * 2, 256);
     w->vexp = w->partial + round_up(static_cast<size_t>(heads) * w->chunks * sizeof(float), 256);
-    w->total = w->vexp + round_up(static_cast<size_t>(heads) * sizeof(int32_t), 256);
+    w->boff = w->vexp + round_up(static_cast<size_t>(heads) * sizeof(int32_t), 256);
+    w->flags = w->boff + round_up(static_cast<size_t>(B + 1) * sizeof(long long), 256);
+    w->part = w->flags + round_up(8 * attn_impl::SCHED_MAX_CTAS * sizeof(unsigned int), 256);
+    w->total = w->part + round_up(static_cast<size_t>(attn_impl::SCHED_MAX_CTAS) * 2 * (d + 2) * 128 * sizeof(float), 256);
     return w->chunks <= 65535 && heads <= 65535;
+}
+
+// SM count of the current device (cached per device).
+int device_sms() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+    if (dev < 64) {
+        const int c = cache[dev].load();
+        if (c > 0) return c;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return -1;
+    if (dev < 64) cache[dev].store(sms);
+    return sms;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -119,6 +141,7 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     // bf16 inputs: tensor-core path
     WorkspaceLayout w;
     if (!workspace_layout(B, H_kv, N, d, &w)) return ATTN_ERR_UNSUPPORTED;
+    if (attn_impl::plan_max_steps(B, H, N, causal) >= 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total) return ATTN_ERR_INVALID_ARG;
     if (!get_encoder()) return ATTN_ERR_CUDA;
 
@@ -138,19 +161,30 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
         !encode_rows_map(&tmV, vp.V16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, d, N, static_cast<long long>(B) * H_kv))
         return ATTN_ERR_UNSUPPORTED;
 
+    const int sms = device_sms();
+    if (sms <= 0) return ATTN_ERR_CUDA;
     attn_impl::TcParams p{};
     p.O = O;
     p.LSE = LSE;
     p.kv_len = kv_len;
     p.v_exp = vp.v_exp;
-    p.B = B; p.H = H; p.H_kv = H_kv; p.N = N; p.group = H / H_kv;
-    p.n_pairs = (N + 255) / 256;
-    p.causal = causal;
+    p.boff = reinterpret_cast<const long long*>(ws + w.boff);
+    p.part = reinterpret_cast<float*>(ws + w.part);
+    p.flags = reinterpret_cast<unsigned int*>(ws + w.flags);
+    p.plan = attn_impl::make_plan(B, H, N, causal, kv_len != nullptr, sms);
+    p.H_kv = H_kv;
+    p.group = H / H_kv;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.wait_limit_ns = g_wait_limit_ns.load();
     p.debug_skip_kv_load = g_skip_kv_load.load();
 
-    if (attn_impl::launch_vprep(vp, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    attn_impl::PlanParams pl{};
+    pl.kv_len = kv_len;
+    pl.boff = reinterpret_cast<long long*>(ws + w.boff);
+    pl.flags = p.flags;
+    pl.B = B; pl.H = H; pl.N = N; pl.n_pairs = p.plan.n_pairs; pl.causal = causal;
+
+    if (attn_impl::launch_vprep(vp, pl, stream) != cudaSuccess) return ATTN_ERR_CUDA;
     cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
     const bool timed = ev0 && ev1;
     if (timed && cudaEventRecord(ev0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -163,8 +197,11 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
 attn_status attn_check(cudaStream_t stream) {
     uint32_t bits = 0;
     if (attn_impl::read_and_clear_error(&bits, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    g_last_error_bits.store(bits);
     return bits ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
+
+uint32_t attn_debug_last_error_bits(void) { return g_last_error_bits.load(); }
 
 const char* attn_status_string(attn_status s) {
     switch (s) {
@@ -182,6 +219,37 @@ int attn_launches_per_call(attn_dtype in_dtype) { return in_dtype == ATTN_BF16 ?
 void attn_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs); }
 
 void attn_debug_set_skip_kv_load(int on) { g_skip_kv_load.store(on ? 1 : 0); }
+
+int attn_debug_schedule(int B, int H, int N, int causal, const int32_t* kv_len_host, int sms, int32_t* out,
+                        int max_segments) {
+    if (B <= 0 || H <= 0 || N <= 0 || sms <= 0 || max_segments < 0 || (!out && max_segments > 0)) return -1;
+    if (attn_impl::plan_max_steps(B, H, N, causal ? 1 : 0) >= 0x7fffffffLL) return -1;
+    const attn_impl::SchedPlan plan = attn_impl::make_plan(B, H, N, causal ? 1 : 0, kv_len_host != nullptr, sms);
+    std::vector<int> nb(B);
+    std::vector<long long> boff(B + 1, 0);
+    for (int b = 0; b < B; ++b) {
+        int L = kv_len_host ? kv_len_host[b] : N;
+        L = L < 0 ? 0 : (L > N ? N : L);
+        nb[b] = attn_impl::key_tiles(L);
+        boff[b + 1] = boff[b] + static_cast<long long>(H) * attn_impl::pair_prefix(plan.n_pairs, nb[b], N, plan.causal);
+    }
+    const attn_impl::HostSchedTab tab{nb.data(), boff.data()};
+    int n = 0;
+    for (int c = 0; c < plan.G; ++c) {
+        attn_impl::WalkState walk;
+        attn_impl::walk_init(walk, tab, plan);
+        attn_impl::Segment sg;
+        while (attn_impl::walk_next(walk, tab, plan, c, sg)) {
+            if (n < max_segments) {
+                int32_t* o = out + 8 * static_cast<size_t>(n);
+                o[0] = c; o[1] = sg.b; o[2] = sg.h; o[3] = sg.pair; o[4] = sg.k0; o[5] = sg.k1; o[6] = sg.cost;
+                o[7] = sg.kind;
+            }
+            ++n;
+        }
+    }
+    return n;
+}
 
 float attn_event_elapsed_ms(cudaEvent_t start, cudaEvent_t stop) {
     float ms = -1.f;

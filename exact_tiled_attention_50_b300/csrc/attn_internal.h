@@ -17,6 +17,170 @@ enum : uint32_t {
     ERRBIT_WAIT_O = 32u,
     ERRBIT_WAIT_EMPTY = 64u,
     ERRBIT_WAIT_DRAIN = 128u,
+    ERRBIT_WAIT_PART = 256u,    // an owner CTA waited for another CTA's partial result
+};
+
+// ---------------------------------------------------------------------------------------------
+// Work schedule of the persistent tensor-core kernel (host and device code share it).
+//
+// A work unit is (b, h, pair): 256 query rows (two 128-row query tiles) of one head. Its cost is the
+// number of 128-key steps it needs: the larger of its two tiles' key-tile counts below
+// min(kv_len[b], causal limit), and at least 1 (a unit without any valid key still writes O = 0,
+// LSE = -inf). Units lie on a line in (b, h, pair) order; unit u covers [off(u), off(u) + cost(u)).
+// CTA c of G first runs R_dp data-parallel rounds (unit r*G + c in round r; used only when every unit
+// has the same cost), then one contiguous chunk of the rest of the line,
+// [S0 + (W - S0) c / G, S0 + (W - S0) (c + 1) / G). A unit that a chunk boundary cuts is computed in
+// pieces over disjoint key ranges. The piece that holds the unit's first key step (the owner) is the
+// last segment of its CTA; the other pieces are the first segments of the following CTAs' chunks,
+// which write their partial results (unnormalised O, running max m, running sum l) to a slot of
+// their own. The owner merges them with the softmax merge rule: m = max(m_a, m_b),
+// O = O_a 2^(m_a - m) + O_b 2^(m_b - m), l = l_a 2^(m_a - m) + l_b 2^(m_b - m), then O / l.
+// ---------------------------------------------------------------------------------------------
+constexpr int SCHED_MAX_CTAS = 160;  // partial-result slots reserved in the workspace
+constexpr int SCHED_MIN_STEPS = 2;   // the CTA count is capped so that chunks hold at least this many steps
+
+enum : int { SEG_COMPLETE = 0, SEG_OWNER = 1, SEG_WRITER = 2 };
+
+__host__ __device__ inline int key_tiles(int kv_valid) { return (kv_valid + 127) / 128; }
+
+// Sum of the costs of pairs [0, P) of one head in a batch with nb valid key tiles.
+__host__ __device__ inline long long pair_prefix(int P, int nb, int N, int causal) {
+    if (nb <= 0) return P;  // units without keys cost 1 each
+    if (!causal) return static_cast<long long>(P) * nb;
+    const int n_full = N > 128 ? (N - 129) / 256 + 1 : 0;  // pairs whose second tile exists
+    const int Pf = P < n_full ? P : n_full;
+    const int half = nb / 2;
+    const long long k = Pf < half ? Pf : half;  // pairs p with 2p + 2 <= nb cost 2p + 2
+    long long s = k * (k + 1) + static_cast<long long>(Pf - k) * nb;  // the rest cost nb
+    if (P > n_full) s += (nb < 2 * n_full + 1 ? nb : 2 * n_full + 1);  // last pair: its first tile only
+    return s;
+}
+
+__host__ __device__ inline int pair_cost(int pair, int nb, int N, int causal) {
+    return static_cast<int>(pair_prefix(pair + 1, nb, N, causal) - pair_prefix(pair, nb, N, causal));
+}
+
+struct SchedPlan {
+    int B, H, N, n_pairs, causal;
+    int G;          // persistent CTAs
+    int R_dp;       // data-parallel rounds
+    int S0;         // line offset where the stream-K part starts (the whole line is below 2^31)
+};
+
+struct Segment {
+    int b, h, pair;
+    int k0, k1;          // key steps [k0, k1) of the unit
+    int cost;            // the unit's cost
+    int unit_end;        // line offset just past the unit
+    int kind;            // SEG_COMPLETE, SEG_OWNER or SEG_WRITER
+};
+
+__host__ __device__ inline int sched_chunk_start(const SchedPlan& p, int W, int c) {
+    return p.S0 + static_cast<int>(static_cast<long long>(W - p.S0) * c / p.G);
+}
+
+// Enumerates the segments of CTA `cta` in the order it runs them (walk_init once, then walk_next
+// until it returns false). Tab provides
+//   int nb(int b)              valid key tiles of batch b
+//   long long boff(int b)      line offset of batch b's first unit, b = 0..B (boff(B) = W < 2^31)
+// The state is a plain struct so that the kernel can keep it in shared memory, out of the registers
+// of the roles that walk it.
+struct WalkState {
+    int W, round, sk_started, pos, chunk_end, unit_off, b, h, pair;
+};
+
+template <class Tab>
+__host__ __device__ inline void walk_init(WalkState& w, const Tab& t, const SchedPlan& p) {
+    w.W = static_cast<int>(t.boff(p.B));
+    w.round = 0;
+    w.sk_started = 0;
+    w.pos = w.chunk_end = w.unit_off = 0;
+    w.b = w.h = w.pair = 0;
+}
+
+template <class Tab>
+__host__ __device__ inline int walk_head_cost(const Tab& t, const SchedPlan& p, int b) {
+    return static_cast<int>(pair_prefix(p.n_pairs, t.nb(b), p.N, p.causal));
+}
+
+// b, h, pair and unit_off of the unit that contains line position x (boff(0) <= x < W)
+template <class Tab>
+__host__ __device__ inline void walk_locate(WalkState& w, const Tab& t, const SchedPlan& p, int x) {
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {  // largest b with boff(b) <= x
+        const int mid = (lo + hi + 1) / 2;
+        if (t.boff(mid) <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    w.b = lo;
+    const int nb = t.nb(lo);
+    const int hc = walk_head_cost(t, p, lo);
+    const int rem = x - static_cast<int>(t.boff(lo));
+    w.h = rem / hc;
+    const int r2 = rem - w.h * hc;
+    int plo = 0, phi = p.n_pairs - 1;
+    while (plo < phi) {  // largest pair with pair_prefix(pair) <= r2
+        const int mid = (plo + phi + 1) / 2;
+        if (pair_prefix(mid, nb, p.N, p.causal) <= r2) plo = mid;
+        else phi = mid - 1;
+    }
+    w.pair = plo;
+    w.unit_off = static_cast<int>(t.boff(lo)) + w.h * hc + static_cast<int>(pair_prefix(plo, nb, p.N, p.causal));
+}
+
+template <class Tab>
+__host__ __device__ inline bool walk_next(WalkState& w, const Tab& t, const SchedPlan& p, int cta, Segment& s) {
+    if (w.round < p.R_dp) {
+        const long long u = static_cast<long long>(w.round) * p.G + cta;
+        ++w.round;
+        const long long per_b = static_cast<long long>(p.H) * p.n_pairs;
+        s.b = static_cast<int>(u / per_b);
+        s.h = static_cast<int>((u / p.n_pairs) % p.H);
+        s.pair = static_cast<int>(u % p.n_pairs);
+        const int nb = t.nb(s.b);
+        s.cost = pair_cost(s.pair, nb, p.N, p.causal);
+        s.k0 = 0;
+        s.k1 = s.cost;
+        s.unit_end = static_cast<int>(t.boff(s.b)) + s.h * walk_head_cost(t, p, s.b) +
+                     static_cast<int>(pair_prefix(s.pair + 1, nb, p.N, p.causal));
+        s.kind = SEG_COMPLETE;
+        return true;
+    }
+    if (!w.sk_started) {
+        w.sk_started = 1;
+        w.pos = sched_chunk_start(p, w.W, cta);
+        w.chunk_end = sched_chunk_start(p, w.W, cta + 1);
+        if (w.pos < w.chunk_end) walk_locate(w, t, p, w.pos);
+    }
+    if (w.pos >= w.chunk_end) return false;
+    const int cost = pair_cost(w.pair, t.nb(w.b), p.N, p.causal);
+    const int end = w.unit_off + cost;
+    s.b = w.b;
+    s.h = w.h;
+    s.pair = w.pair;
+    s.cost = cost;
+    s.k0 = w.pos - w.unit_off;
+    s.k1 = (w.chunk_end < end ? w.chunk_end : end) - w.unit_off;
+    s.unit_end = end;
+    s.kind = s.k0 > 0 ? SEG_WRITER : (s.k1 < cost ? SEG_OWNER : SEG_COMPLETE);
+    w.pos = w.unit_off + s.k1;
+    w.unit_off = end;
+    if (++w.pair == p.n_pairs) {
+        w.pair = 0;
+        if (++w.h == p.H) {
+            w.h = 0;
+            ++w.b;
+        }
+    }
+    return true;
+}
+
+// Host-side table over arrays (the schedule check of the test hook).
+struct HostSchedTab {
+    const int* nb_;
+    const long long* boff_;
+    __host__ __device__ int nb(int b) const { return nb_[b]; }
+    __host__ __device__ long long boff(int b) const { return boff_[b]; }
 };
 
 struct TcParams {
@@ -24,13 +188,22 @@ struct TcParams {
     float* LSE;               // [B,H,N] or nullptr
     const int32_t* kv_len;    // [B] or nullptr
     const int32_t* v_exp;     // [B*H_kv] power-of-two exponent of the fp16 copy of V
-    int B, H, H_kv, N;
+    const long long* boff;    // [B+1] line offset of each batch's first unit (plan pass)
+    float* part;              // partial results [G][2][D + 2][128] (O columns, then m, then l; row fastest)
+    unsigned int* flags;      // [G][2][4] partial-result ready flags (per CTA, tile, warp), zeroed by the plan pass
+    SchedPlan plan;
+    int H_kv;
     int group;                // H / H_kv
-    int n_pairs;              // ceil(N / 256): CTA work units per (b, h)
-    int causal;
     float scale_log2;         // scale * log2(e)
     unsigned long long wait_limit_ns;
     int debug_skip_kv_load;
+};
+
+struct PlanParams {
+    const int32_t* kv_len;
+    long long* boff;          // [B+1]
+    unsigned int* flags;      // [8 * SCHED_MAX_CTAS]
+    int B, H, N, n_pairs, causal;
 };
 
 struct F32Params {
@@ -57,9 +230,13 @@ struct VPrepParams {
 
 constexpr int VPREP_CHUNK = 16384;  // elements of V per CTA in the fp16 conversion
 
-cudaError_t launch_vprep(const VPrepParams& p, cudaStream_t stream);
+cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStream_t stream);
 cudaError_t launch_attn_tc(int d, bool out_bf16, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmV16, const TcParams& p, cudaStream_t stream);
+
+// Persistent-CTA plan for these sizes on a device with `sms` SMs (kv_len given or not).
+SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms);
+long long plan_max_steps(int B, int H, int N, int causal);
 cudaError_t launch_attn_f32(int d, const F32Params& p, cudaStream_t stream);
 
 // Device error word of the current device: read and clear (synchronous on `stream`).

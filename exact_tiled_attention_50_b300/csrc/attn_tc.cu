@@ -72,12 +72,12 @@ constexpr int TMA_WARP = 9;
 constexpr float RESCALE_THRESHOLD = 15.0f;
 constexpr uint32_t TMEM_COLS = 512;
 // Register split: the block launches with 384 x 168 = 64512 registers; the two softmax
-// warpgroups raise theirs to 208 and the MMA/TMA warpgroup lowers its to 88:
-// 2*128*208 + 128*88 = 64512 (every sub-partition holds two softmax warps and one other warp:
-// 2*208 + 88 = 504 <= 512 registers per lane).
+// warpgroups raise theirs to 200 and the MMA/TMA warpgroup lowers its to 104:
+// 2*128*200 + 128*104 = 64512 (every sub-partition holds two softmax warps and one other warp:
+// 2*200 + 104 = 504 <= 512 registers per lane).
 constexpr int LAUNCH_REGS = 168;
-constexpr uint32_t SOFTMAX_REGS = 208;
-constexpr uint32_t CONTROL_REGS = 88;
+constexpr uint32_t SOFTMAX_REGS = 200;
+constexpr uint32_t CONTROL_REGS = 104;
 static_assert(2 * 128 * SOFTMAX_REGS + 128 * CONTROL_REGS <= NUM_THREADS * LAUNCH_REGS, "register split");
 
 template <int D>
@@ -108,43 +108,78 @@ __device__ __forceinline__ int clamp_len(const int32_t* kv_len, int b, int N) {
 
 }  // namespace
 
+// Schedule table on the device: kv_len from the caller, batch offsets from the plan pass; reads the
+// kernel's grid-constant parameter in place.
+struct DevSchedTab {
+    const TcParams& p;
+    __device__ int nb(int b) const { return key_tiles(clamp_len(p.kv_len, b, p.plan.N)); }
+    __device__ long long boff(int b) const { return p.boff[b]; }
+};
+
+// Per-segment quantities every role derives the same way.
+struct SegInfo {
+    int bh, zkv;
+    int q0[2];       // first query row of each tile
+    int n[2];        // key steps of each tile inside this piece
+    int nmax;
+    int kv_valid;
+};
+
+__device__ __forceinline__ SegInfo seg_info(const TcParams& p, const Segment& s) {
+    SegInfo si;
+    const int N = p.plan.N;
+    si.kv_valid = clamp_len(p.kv_len, s.b, N);
+    si.bh = s.b * p.plan.H + s.h;
+    si.zkv = s.b * p.H_kv + s.h / p.group;
+    si.nmax = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int q0 = s.pair * 2 * BLOCK_M + t * BLOCK_M;
+        si.q0[t] = q0;
+        const int lim = p.plan.causal ? min(si.kv_valid, q0 + BLOCK_M) : si.kv_valid;
+        const int nkv = q0 < N ? key_tiles(lim) : 0;
+        const int hi = min(s.k1, nkv);
+        si.n[t] = hi > s.k0 ? hi - s.k0 : 0;
+        si.nmax = max(si.nmax, si.n[t]);
+    }
+    return si;
+}
+
 template <int D, bool OUT_BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ TcParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    __shared__ __align__(8) uint64_t bar_q;                 // Q_0, Q_1 and K_0 landed
+    __shared__ __align__(8) uint64_t bar_q;                 // Q_0, Q_1 and the segment's first K landed
+    __shared__ __align__(8) uint64_t bar_q_empty;           // every MMA of the segment completed
     __shared__ __align__(8) uint64_t bar_full[C::NP];       // ring stage (V_j, K_j+1) landed
     __shared__ __align__(8) uint64_t bar_empty[C::NP];      // ring stage free again
     __shared__ __align__(8) uint64_t bar_s_full[2];         // S_t in TMEM
     __shared__ __align__(8) uint64_t bar_p_full[2][2];      // half h of P_t in TMEM (O_t rescaled)
-    __shared__ __align__(8) uint64_t bar_o_full[2];         // last P V into O_t done
+    __shared__ __align__(8) uint64_t bar_o_full[2];         // last P V of the segment into O_t done
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
+    // Work-schedule walkers, one per working warp (warps 0-9), advanced by one lane; the current
+    // segment is read from shared memory so that the walker state stays out of registers.
+    __shared__ WalkState walk_sh[10];
+    __shared__ Segment seg_sh[10];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- work unit: (b, h, pair of 128-row query tiles); causal: heaviest pairs launch first ----
-    const int BH = p.B * p.H;
-    const int bh = blockIdx.x % BH;
-    const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x / BH);
-    const int b = bh / p.H;
-    const int h = bh - b * p.H;
-    const int zkv = b * p.H_kv + h / p.group;
-    const int kv_valid = clamp_len(p.kv_len, b, p.N);
-    // query tile t covers rows [q0_t, q0_t + 128); it needs key tiles [0, nkv_t)
-    auto tile_nkv = [&](int q0) {
-        const int limit = p.causal ? min(kv_valid, q0 + BLOCK_M) : kv_valid;
-        return q0 < p.N ? (limit + BLOCK_N - 1) / BLOCK_N : 0;
+    const DevSchedTab tab{p};
+    if (warp < 10 && lane == 0) walk_init(walk_sh[warp], tab, p.plan);
+    // warp-collective: the next segment of this warp's walker into seg_sh[warp]
+    auto next_seg = [&]() -> bool {
+        int more = 0;
+        if (lane == 0) more = walk_next(walk_sh[warp], tab, p.plan, static_cast<int>(blockIdx.x), seg_sh[warp]);
+        more = __shfl_sync(0xffffffffu, more, 0);
+        __syncwarp();
+        return more != 0;
     };
-    const int q0_0 = 2 * pair * BLOCK_M, q0_1 = q0_0 + BLOCK_M;
-    const int nkv_0 = tile_nkv(q0_0), nkv_1 = tile_nkv(q0_1);
-    const int nmax = max(nkv_0, nkv_1);
 
     // ---- setup ----
     if (warp == MMA_WARP) {
@@ -153,6 +188,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (threadIdx.x == TMA_WARP * 32) {
         mbar_init(&bar_q, 1);
+        mbar_init(&bar_q_empty, 1);
         for (int s = 0; s < C::NP; ++s) {
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_empty[s], 1);
@@ -180,56 +216,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // allocator sees the larger budget only where it holds.
     if (warp >= 8) {
         regs_decrease<CONTROL_REGS>();
-        if (warp == TMA_WARP && nmax > 0) {
+        if (warp == TMA_WARP) {
             // ============================== TMA producer (one lane) ==============================
             if (elect_one()) {
                 const uint64_t pol_kv = l2_policy_evict_last();
                 const uint64_t pol_q = l2_policy_evict_first();
-                uint32_t qbytes = C::TILE_BYTES;  // K_0
-                qbytes += nkv_0 > 0 ? C::TILE_BYTES : 0;
-                qbytes += nkv_1 > 0 ? C::TILE_BYTES : 0;
-                mbar_arrive_expect_tx(&bar_q, qbytes);
-#pragma unroll
-                for (int t = 0; t < 2; ++t)
-                    if ((t ? nkv_1 : nkv_0) > 0)
-                        for (int bx = 0; bx < C::NB; ++bx)
-                            tma_load_3d_hint(smem + t * C::TILE_BYTES + bx * 16384, &tmQ, &bar_q, bx * 64,
-                                             t ? q0_1 : q0_0, bh, pol_q);
-                if (!p.debug_skip_kv_load)  // failure-path test: K_0 is never loaded
-                    for (int bx = 0; bx < C::NB; ++bx)
-                        tma_load_3d_hint(smem + C::OFF_K0 + bx * 16384, &tmK, &bar_q, bx * 64, 0, zkv, pol_kv);
-                int issued = 0;
+                WalkState& walk = walk_sh[TMA_WARP];
+                const Segment& s = seg_sh[TMA_WARP];
+                uint32_t g = 0;        // ring steps issued
+                uint32_t segq = 0;     // segments whose Q was issued
                 bool ok = true;
-                for (int j = 0; j < nmax; ++j) {
-                    const int st = j % C::NP;
-                    if (j >= C::NP &&
-                        !mbar_wait(&bar_empty[st], ((j / C::NP) - 1) & 1, limit_ns, &abort_flag)) {
+                bool skip_k = p.debug_skip_kv_load != 0;  // failure-path test: the first K is never loaded
+                while (ok && walk_next(walk, tab, p.plan, static_cast<int>(blockIdx.x), seg_sh[TMA_WARP])) {
+                    const SegInfo si = seg_info(p, s);
+                    if (si.nmax == 0) continue;
+                    if (segq > 0 && !mbar_wait(&bar_q_empty, (segq - 1) & 1, limit_ns, &abort_flag)) {
                         record_failure(&abort_flag, ERRBIT_WAIT_EMPTY);
                         ok = false;
                         break;
                     }
-                    const bool has_k = j + 1 < nmax;
-                    mbar_arrive_expect_tx(&bar_full[st], has_k ? 2 * C::TILE_BYTES : C::TILE_BYTES);
-                    uint8_t* dst = smem + C::OFF_RING + st * C::STAGE_BYTES;
-                    for (int bx = 0; bx < C::NB; ++bx)
-                        tma_load_3d_hint(dst + bx * 16384, &tmV, &bar_full[st], bx * 64, j * BLOCK_N, zkv, pol_kv);
-                    if (has_k)
+                    uint32_t qbytes = C::TILE_BYTES;  // the segment's first K tile
+                    qbytes += si.n[0] > 0 ? C::TILE_BYTES : 0;
+                    qbytes += si.n[1] > 0 ? C::TILE_BYTES : 0;
+                    mbar_arrive_expect_tx(&bar_q, qbytes);
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+                        if (si.n[t] > 0)
+                            for (int bx = 0; bx < C::NB; ++bx)
+                                tma_load_3d_hint(smem + t * C::TILE_BYTES + bx * 16384, &tmQ, &bar_q, bx * 64,
+                                                 si.q0[t], si.bh, pol_q);
+                    if (!skip_k)
                         for (int bx = 0; bx < C::NB; ++bx)
-                            tma_load_3d_hint(dst + C::TILE_BYTES + bx * 16384, &tmK, &bar_full[st], bx * 64,
-                                             (j + 1) * BLOCK_N, zkv, pol_kv);
-                    issued = j + 1;
+                            tma_load_3d_hint(smem + C::OFF_K0 + bx * 16384, &tmK, &bar_q, bx * 64, s.k0 * BLOCK_N,
+                                             si.zkv, pol_kv);
+                    skip_k = false;
+                    ++segq;
+                    const int jend = s.k0 + si.nmax;
+                    for (int j = s.k0; j < jend; ++j) {
+                        const uint32_t st = g % C::NP;
+                        if (g >= C::NP &&
+                            !mbar_wait(&bar_empty[st], ((g / C::NP) - 1) & 1, limit_ns, &abort_flag)) {
+                            record_failure(&abort_flag, ERRBIT_WAIT_EMPTY);
+                            ok = false;
+                            break;
+                        }
+                        const bool has_k = j + 1 < jend;
+                        mbar_arrive_expect_tx(&bar_full[st], has_k ? 2 * C::TILE_BYTES : C::TILE_BYTES);
+                        uint8_t* dst = smem + C::OFF_RING + st * C::STAGE_BYTES;
+                        for (int bx = 0; bx < C::NB; ++bx)
+                            tma_load_3d_hint(dst + bx * 16384, &tmV, &bar_full[st], bx * 64, j * BLOCK_N, si.zkv,
+                                             pol_kv);
+                        if (has_k)
+                            for (int bx = 0; bx < C::NB; ++bx)
+                                tma_load_3d_hint(dst + C::TILE_BYTES + bx * 16384, &tmK, &bar_full[st], bx * 64,
+                                                 (j + 1) * BLOCK_N, si.zkv, pol_kv);
+                        ++g;
+                    }
                 }
                 // On failure, wait (bounded) for the copies this thread issued, so that no TMA write
                 // lands in shared memory after the CTA has exited.
                 if (!ok || abort_flag) {
                     volatile int never = 0;  // these waits must not be cut short by the abort flag
-                    if (!p.debug_skip_kv_load) (void)mbar_wait(&bar_q, 0, limit_ns, &never);
-                    for (int j = issued > C::NP ? issued - C::NP : 0; j < issued; ++j)
-                        (void)mbar_wait(&bar_full[j % C::NP], (j / C::NP) & 1, limit_ns, &never);
+                    if (segq > 0) (void)mbar_wait(&bar_q, (segq - 1) & 1, limit_ns, &never);
+                    for (uint32_t gg = g > C::NP ? g - C::NP : 0; gg < g; ++gg)
+                        (void)mbar_wait(&bar_full[gg % C::NP], (gg / C::NP) & 1, limit_ns, &never);
                 }
             }
             __syncwarp();
-        } else if (warp == MMA_WARP && nmax > 0) {
+        } else if (warp == MMA_WARP) {
             // ======================= MMA issuer (converged warp, one lane issues) =======================
             auto wait_all = [&](uint64_t* bar, uint32_t parity, uint32_t bit) {
                 const bool got = mbar_wait(bar, parity, limit_ns, &abort_flag);
@@ -263,63 +317,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             (accumulate || kk > 0));
                 }
             };
-            bool ok = wait_all(&bar_q, 0, ERRBIT_WAIT_Q);
-            if (ok) {
-                tc_fence_after();
-                if (elect_one()) {
-                    if (nkv_0 > 0) {
-                        issue_S(0, dK0);
-                        umma_commit(&bar_s_full[0]);
-                    }
-                    if (nkv_1 > 0) {
-                        issue_S(1, dK0);
-                        umma_commit(&bar_s_full[1]);
-                    }
-                }
-                __syncwarp();
-            }
-            for (int j = 0; j < nmax && ok; ++j) {
-                const int st = j % C::NP;
-                ATTN_TRACE_AT(0, j, 4);
-                if (!wait_all(&bar_full[st], (j / C::NP) & 1, ERRBIT_WAIT_KV)) {
+            const Segment& s = seg_sh[MMA_WARP];
+            uint32_t g = 0, segq = 0;
+            uint32_t cnt_p[2] = {0u, 0u};
+            bool ok = true;
+            while (ok && next_seg()) {
+                const SegInfo si = seg_info(p, s);
+                if (si.nmax == 0) continue;
+                if (!wait_all(&bar_q, segq & 1, ERRBIT_WAIT_Q)) {
                     ok = false;
                     break;
                 }
+                ++segq;
                 tc_fence_after();
-                ATTN_TRACE_AT(0, j, 5);
-                const uint64_t dv = dRingV + static_cast<uint64_t>((st * C::STAGE_BYTES) >> 4);
-                const uint64_t dk = dRingK + static_cast<uint64_t>((st * C::STAGE_BYTES) >> 4);
+                if (elect_one()) {
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const int n_t = t ? nkv_1 : nkv_0;
-                    if (!ok || j >= n_t) continue;
-                    if (!wait_all(&bar_p_full[t][0], j & 1, ERRBIT_WAIT_P)) {
-                        ok = false;
-                        continue;
-                    }
-                    tc_fence_after();
-                    ATTN_TRACE_AT(0, j, 2 * t);
-                    if (elect_one()) issue_PV_half(t, dv, 0, j > 0);
-                    __syncwarp();
-                    if (!wait_all(&bar_p_full[t][1], j & 1, ERRBIT_WAIT_P)) {
-                        ok = false;
-                        continue;
-                    }
-                    tc_fence_after();
-                    if (elect_one()) {
-                        issue_PV_half(t, dv, 1, true);
-                        if (j + 1 < n_t) {
-                            issue_S(t, dk);
+                    for (int t = 0; t < 2; ++t)
+                        if (si.n[t] > 0) {
+                            issue_S(t, dK0);
                             umma_commit(&bar_s_full[t]);
-                        } else {
-                            umma_commit(&bar_o_full[t]);
                         }
+                }
+                __syncwarp();
+                for (int jj = 0; jj < si.nmax; ++jj) {
+                    const uint32_t st = g % C::NP;
+                    ATTN_TRACE_AT(0, g, 4);
+                    if (!wait_all(&bar_full[st], (g / C::NP) & 1, ERRBIT_WAIT_KV)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    ATTN_TRACE_AT(0, g, 5);
+                    const uint64_t dv = dRingV + static_cast<uint64_t>((st * C::STAGE_BYTES) >> 4);
+                    const uint64_t dk = dRingK + static_cast<uint64_t>((st * C::STAGE_BYTES) >> 4);
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (!ok || jj >= si.n[t]) continue;
+                        if (!wait_all(&bar_p_full[t][0], cnt_p[t] & 1, ERRBIT_WAIT_P)) {
+                            ok = false;
+                            continue;
+                        }
+                        tc_fence_after();
+                        ATTN_TRACE_AT(0, g, 2 * t);
+                        if (elect_one()) issue_PV_half(t, dv, 0, jj > 0);
+                        __syncwarp();
+                        if (!wait_all(&bar_p_full[t][1], cnt_p[t] & 1, ERRBIT_WAIT_P)) {
+                            ok = false;
+                            continue;
+                        }
+                        ++cnt_p[t];
+                        tc_fence_after();
+                        if (elect_one()) {
+                            issue_PV_half(t, dv, 1, true);
+                            if (jj + 1 < si.n[t]) {
+                                issue_S(t, dk);
+                                umma_commit(&bar_s_full[t]);
+                            } else {
+                                umma_commit(&bar_o_full[t]);
+                            }
+                        }
+                        __syncwarp();
+                        ATTN_TRACE_AT(0, g, 2 * t + 1);
+                    }
+                    if (!ok) break;
+                    if (elect_one()) umma_commit(&bar_empty[st]);
                     __syncwarp();
-                    ATTN_TRACE_AT(0, j, 2 * t + 1);
+                    ++g;
                 }
                 if (!ok) break;
-                if (elect_one()) umma_commit(&bar_empty[st]);
+                // Q and the first K of this segment may be overwritten once these MMAs completed
+                if (elect_one()) umma_commit(&bar_q_empty);
                 __syncwarp();
             }
             // Drain: every MMA this warp issued has completed before tensor memory is freed.
@@ -335,150 +402,222 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int t = warp >> 2;            // query tile of this warpgroup
         const int wq = warp & 3;            // TMEM lane quarter
         const int r = wq * 32 + lane;       // row within the tile
-        const int q0t = t ? q0_1 : q0_0;
-        const int nkvt = t ? nkv_1 : nkv_0;
-        const int row = q0t + r;            // query index
         const uint32_t lane_off = tmem_lane_base(wq);
         const uint32_t tS = tmem + lane_off + t * BLOCK_N;
         const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
         const float sl = p.scale_log2;
-        float m_run = -INFINITY;            // reference maximum (log2 domain, already scaled)
-        float l_run = 0.f;                  // running sum of exp2(s*sl - m_run)
-        bool ok = true;
-        const int row_lim = p.causal ? min(kv_valid, row + 1) : kv_valid;  // keys < row_lim are valid
         const bool trace_me = (threadIdx.x & 127) == 0;
+        const int G = p.plan.G;
+        const Segment& s = seg_sh[warp];
+        uint32_t cnt_s = 0, cnt_o = 0;
+        bool ok = true;
 
-        for (int j = 0; j < nkvt; ++j) {
-            // tcgen05.ld/st below are warp-collective: the warp proceeds only if every lane's wait
-            // succeeded
-            if (trace_me) ATTN_TRACE_AT(1 + t, j, 0);
-            const bool got = mbar_wait(&bar_s_full[t], j & 1, limit_ns, &abort_flag);
-            if (!__all_sync(0xffffffffu, got)) {
-                if (!got) record_failure(&abort_flag, ERRBIT_WAIT_S);
-                ok = false;
-                break;
+        while (ok && next_seg()) {
+            // only what the key loop needs stays in registers; the rest is re-read from shared memory
+            const int k0 = s.k0;
+            const int q0t = s.pair * 2 * BLOCK_M + t * BLOCK_M;
+            const int kv_valid = clamp_len(p.kv_len, s.b, p.plan.N);
+            int nkvt = 0;
+            if (q0t < p.plan.N) {
+                const int hi = min(s.k1, key_tiles(p.plan.causal ? min(kv_valid, q0t + BLOCK_M) : kv_valid));
+                nkvt = hi > k0 ? hi - k0 : 0;
             }
-            tc_fence_after();
-            if (trace_me) ATTN_TRACE_AT(1 + t, j, 1);
-            uint32_t ra[32], rb[32], rc[32], rd[32];
-            tmem_ld32(tS + 0, ra);
-            tmem_ld32(tS + 32, rb);
-            tmem_ld32(tS + 64, rc);
-            tmem_ld32(tS + 96, rd);
-            tmem_wait_ld(ra);
-            tmem_wait_ld(rb);
-            tmem_wait_ld(rc);
-            tmem_wait_ld(rd);
-            if (trace_me) ATTN_TRACE_AT(1 + t, j, 2);
-            float x[128];
+            const int row = q0t + r;                   // query index
+            const int row_lim = p.plan.causal ? min(kv_valid, row + 1) : kv_valid;  // keys < row_lim are valid
+            float m_run = -INFINITY;                   // reference maximum (log2 domain, already scaled)
+            float l_run = 0.f;                         // running sum of exp2(s*sl - m_run)
+
+            for (int jj = 0; jj < nkvt; ++jj) {
+                const int j = k0 + jj;
+                // tcgen05.ld/st below are warp-collective: the warp proceeds only if every lane's wait
+                // succeeded
+                if (trace_me) ATTN_TRACE_AT(1 + t, j, 0);
+                const bool got = mbar_wait(&bar_s_full[t], cnt_s & 1, limit_ns, &abort_flag);
+                ++cnt_s;
+                if (!__all_sync(0xffffffffu, got)) {
+                    if (!got) record_failure(&abort_flag, ERRBIT_WAIT_S);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (trace_me) ATTN_TRACE_AT(1 + t, j, 1);
+                uint32_t ra[32], rb[32], rc[32], rd[32];
+                tmem_ld32(tS + 0, ra);
+                tmem_ld32(tS + 32, rb);
+                tmem_ld32(tS + 64, rc);
+                tmem_ld32(tS + 96, rd);
+                tmem_wait_ld(ra);
+                tmem_wait_ld(rb);
+                tmem_wait_ld(rc);
+                tmem_wait_ld(rd);
+                if (trace_me) ATTN_TRACE_AT(1 + t, j, 2);
+                float x[128];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                x[i] = __uint_as_float(ra[i]);
-                x[32 + i] = __uint_as_float(rb[i]);
-                x[64 + i] = __uint_as_float(rc[i]);
-                x[96 + i] = __uint_as_float(rd[i]);
-            }
-            const int k0 = j * BLOCK_N;
-            if (k0 + BLOCK_N > kv_valid || (p.causal && k0 + BLOCK_N - 1 > q0t)) {
-                const int lim = row_lim - k0;
+                for (int i = 0; i < 32; ++i) {
+                    x[i] = __uint_as_float(ra[i]);
+                    x[32 + i] = __uint_as_float(rb[i]);
+                    x[64 + i] = __uint_as_float(rc[i]);
+                    x[96 + i] = __uint_as_float(rd[i]);
+                }
+                const int key0 = j * BLOCK_N;
+                if (key0 + BLOCK_N > kv_valid || (p.plan.causal && key0 + BLOCK_N - 1 > q0t)) {
+                    const int lim = row_lim - key0;
 #pragma unroll
-                for (int i = 0; i < 128; ++i)
-                    if (i >= lim) x[i] = -INFINITY;
-            }
-            // row maximum: four independent chains of three-input maxima
-            float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+                    for (int i = 0; i < 128; ++i)
+                        if (i >= lim) x[i] = -INFINITY;
+                }
+                // row maximum: four independent chains of three-input maxima
+                float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-            for (int i = 4; i < 128; i += 8) {
-                mx0 = max3f(mx0, x[i], x[i + 1]);
-                mx1 = max3f(mx1, x[i + 2], x[i + 3]);
-                mx2 = max3f(mx2, x[i + 4], x[i + 5]);
-                mx3 = max3f(mx3, x[i + 6], x[i + 7]);
-            }
-            const float m_tile = max3f(mx0, mx1, fmaxf(mx2, mx3)) * sl;
-            float alpha = 1.f;
-            bool rescale = false;
-            if (j == 0) {
-                m_run = m_tile;
-            } else if (m_tile > m_run + RESCALE_THRESHOLD) {
-                alpha = ex2_approx(m_run - m_tile);
-                l_run *= alpha;
-                m_run = m_tile;
-                rescale = true;
-            }
-            // Lazy rescale of O_t before any of this tile's P V lands in it (the previous P V into
-            // O_t has completed: its completion preceded the S_t commit this warpgroup waited on).
-            if (__any_sync(0xffffffffu, rescale)) {
-                const f32x2 al2 = make_f32x2(alpha, alpha);
+                for (int i = 4; i < 128; i += 8) {
+                    mx0 = max3f(mx0, x[i], x[i + 1]);
+                    mx1 = max3f(mx1, x[i + 2], x[i + 3]);
+                    mx2 = max3f(mx2, x[i + 4], x[i + 5]);
+                    mx3 = max3f(mx3, x[i + 6], x[i + 7]);
+                }
+                const float m_tile = max3f(mx0, mx1, fmaxf(mx2, mx3)) * sl;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (jj == 0) {
+                    m_run = m_tile;
+                } else if (m_tile > m_run + RESCALE_THRESHOLD) {
+                    alpha = ex2_approx(m_run - m_tile);
+                    l_run *= alpha;
+                    m_run = m_tile;
+                    rescale = true;
+                }
+                // Lazy rescale of O_t before any of this tile's P V lands in it (the previous P V into
+                // O_t has completed: its completion preceded the S_t commit this warpgroup waited on).
+                if (__any_sync(0xffffffffu, rescale)) {
+                    const f32x2 al2 = make_f32x2(alpha, alpha);
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c * 32, o);
-                    tmem_wait_ld(o);
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_wait_ld(o);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float a0, a1;
-                        split_f32x2(mul_f32x2(make_f32x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
-                                              al2),
-                                    a0, a1);
-                        o[2 * i] = __float_as_uint(a0);
-                        o[2 * i + 1] = __float_as_uint(a1);
+                        for (int i = 0; i < 16; ++i) {
+                            float a0, a1;
+                            split_f32x2(
+                                mul_f32x2(make_f32x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), al2),
+                                a0, a1);
+                            o[2 * i] = __float_as_uint(a0);
+                            o[2 * i + 1] = __float_as_uint(a1);
+                        }
+                        tmem_st32(tO + c * 32, o);
                     }
-                    tmem_st32(tO + c * 32, o);
                 }
-            }
-            if (trace_me) ATTN_TRACE_AT(1 + t, j, 3);
-            const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
-            // P = exp2(s * scale*log2e - m), written to TMEM as fp16 pairs over the first 64 columns
-            // of S_t, one half (64 keys) at a time; each half is announced as soon as it is stored.
-            // The scale-and-subtract and the row sum use two-wide fp32 instructions.
-            {
-                const f32x2 sl2 = make_f32x2(sl, sl);
-                const f32x2 nm2 = make_f32x2(-m_sub, -m_sub);
-                f32x2 acc0 = make_f32x2(0.f, 0.f), acc1 = acc0;
+                if (trace_me) ATTN_TRACE_AT(1 + t, j, 3);
+                const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
+                // P = exp2(s * scale*log2e - m), written to TMEM as fp16 pairs over the first 64 columns
+                // of S_t, one half (64 keys) at a time; each half is announced as soon as it is stored.
+                // The scale-and-subtract and the row sum use two-wide fp32 instructions.
+                {
+                    const f32x2 sl2 = make_f32x2(sl, sl);
+                    const f32x2 nm2 = make_f32x2(-m_sub, -m_sub);
+                    f32x2 acc0 = make_f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t pk[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float e0, e1;
-                        split_f32x2(fma_f32x2(make_f32x2(x[64 * half + 2 * i], x[64 * half + 2 * i + 1]), sl2, nm2),
-                                    e0, e1);
-                        e0 = ex2_approx(e0);
-                        e1 = ex2_approx(e1);
-                        const f32x2 e = make_f32x2(e0, e1);
-                        if (i & 1) acc1 = add_f32x2(acc1, e);
-                        else acc0 = add_f32x2(acc0, e);
-                        pk[i] = pack_f16x2(e0, e1);
+                        for (int i = 0; i < 32; ++i) {
+                            float e0, e1;
+                            split_f32x2(
+                                fma_f32x2(make_f32x2(x[64 * half + 2 * i], x[64 * half + 2 * i + 1]), sl2, nm2), e0,
+                                e1);
+                            e0 = ex2_approx(e0);
+                            e1 = ex2_approx(e1);
+                            const f32x2 e = make_f32x2(e0, e1);
+                            if (i & 1) acc1 = add_f32x2(acc1, e);
+                            else acc0 = add_f32x2(acc0, e);
+                            pk[i] = pack_f16x2(e0, e1);
+                        }
+                        tmem_st32(tS + 32 * half, pk);
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(&bar_p_full[t][half]);
+                        if (trace_me) ATTN_TRACE_AT(1 + t, j, 4 + half);
                     }
-                    tmem_st32(tS + 32 * half, pk);
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(&bar_p_full[t][half]);
-                    if (trace_me) ATTN_TRACE_AT(1 + t, j, 4 + half);
+                    float s0, s1, s2, s3;
+                    split_f32x2(acc0, s0, s1);
+                    split_f32x2(acc1, s2, s3);
+                    l_run += (s0 + s1) + (s2 + s3);
                 }
-                float s0, s1, s2, s3;
-                split_f32x2(acc0, s0, s1);
-                split_f32x2(acc1, s2, s3);
-                l_run += (s0 + s1) + (s2 + s3);
+                if (trace_me) ATTN_TRACE_AT(1 + t, j, 6);
             }
-            if (trace_me) ATTN_TRACE_AT(1 + t, j, 6);
-        }
+            if (!ok) break;
 
-        // ---- epilogue: O / l (times the fp16 scale of V), LSE ----
-        if (ok && nkvt > 0) {
-            const bool got = mbar_wait(&bar_o_full[t], 0, limit_ns, &abort_flag);
-            if (!__all_sync(0xffffffffu, got)) {
-                if (!got) record_failure(&abort_flag, ERRBIT_WAIT_O);
-                ok = false;
+            // ---- end of the piece: O_t of this piece is complete once the last P V finished ----
+            const bool have = nkvt > 0;
+            if (have) {
+                const bool got = mbar_wait(&bar_o_full[t], cnt_o & 1, limit_ns, &abort_flag);
+                ++cnt_o;
+                if (!__all_sync(0xffffffffu, got)) {
+                    if (!got) record_failure(&abort_flag, ERRBIT_WAIT_O);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
             }
-            tc_fence_after();
-        }
-        if (q0t < p.N) {
-            const bool have = ok && nkvt > 0;
-            const float vscale = have ? ldexpf(1.0f, __ldg(p.v_exp + zkv)) : 0.f;
-            const float inv = (have && l_run > 0.f) ? vscale / l_run : 0.f;
-            const bool store = row < p.N;
-            const size_t obase = (static_cast<size_t>(bh) * p.N + (store ? row : 0)) * D;
+            const bool live = have && l_run > 0.f;     // this row got weight from this piece
+
+            if (s.kind == SEG_WRITER) {
+                // partial result for the owner of the unit: unnormalised O (row fastest), m, l
+                float* base = p.part + (static_cast<size_t>(blockIdx.x) * 2 + t) * (D + 2) * BLOCK_M;
+                if (have) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_wait_ld(o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) base[(c * 32 + i) * BLOCK_M + r] = __uint_as_float(o[i]);
+                    }
+                }
+                base[D * BLOCK_M + r] = live ? m_run : -INFINITY;
+                base[(D + 1) * BLOCK_M + r] = live ? l_run : 0.f;
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) flag_release(p.flags + (blockIdx.x * 2 + t) * 4 + wq, 1u);
+                continue;
+            }
+            if (q0t >= p.plan.N) continue;              // a tile past the last row: nothing to write
+
+            // COMPLETE or OWNER: gather the partial results of the unit's other pieces (owner only)
+            const int W = walk_sh[warp].W;
+            int c_end = blockIdx.x + 1;
+            float M = live ? m_run : -INFINITY;
+            if (s.kind == SEG_OWNER) {
+                while (c_end < G && sched_chunk_start(p.plan, W, c_end) < s.unit_end) ++c_end;
+                for (int c2 = blockIdx.x + 1; c2 < c_end && ok; ++c2) {
+                    if (sched_chunk_start(p.plan, W, c2 + 1) <= sched_chunk_start(p.plan, W, c2)) continue;
+                    if (!flag_wait(p.flags + (c2 * 2 + t) * 4 + wq, 1u, limit_ns, &abort_flag)) {
+                        record_failure(&abort_flag, ERRBIT_WAIT_PART);
+                        ok = false;
+                        break;
+                    }
+                    const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 2) * BLOCK_M;
+                    if (__ldcg(b2 + (D + 1) * BLOCK_M + r) > 0.f) M = fmaxf(M, __ldcg(b2 + D * BLOCK_M + r));
+                }
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+            }
+            const float w_own = live ? ex2_approx(m_run - M) : 0.f;
+            float L = w_own * l_run;
+            for (int c2 = blockIdx.x + 1; c2 < c_end; ++c2) {
+                const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 2) * BLOCK_M;
+                if (sched_chunk_start(p.plan, W, c2 + 1) <= sched_chunk_start(p.plan, W, c2)) continue;
+                const float l2 = __ldcg(b2 + (D + 1) * BLOCK_M + r);
+                if (l2 > 0.f) L += ex2_approx(__ldcg(b2 + D * BLOCK_M + r) - M) * l2;
+            }
+            const int bh = s.b * p.plan.H + s.h;
+            const int zkv = s.b * p.H_kv + s.h / p.group;
+            const float vscale = ldexpf(1.0f, __ldg(p.v_exp + zkv));
+            const float inv = L > 0.f ? vscale / L : 0.f;
+            const bool store = row < p.plan.N;
+            const size_t obase = (static_cast<size_t>(bh) * p.plan.N + (store ? row : 0)) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -488,6 +627,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                // o holds the merged, still unnormalised row values (fp32 bits)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(have ? __uint_as_float(o[i]) * w_own : 0.f);
+                for (int c2 = blockIdx.x + 1; c2 < c_end; ++c2) {
+                    if (sched_chunk_start(p.plan, W, c2 + 1) <= sched_chunk_start(p.plan, W, c2)) continue;
+                    const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 2) * BLOCK_M;
+                    if (!(__ldcg(b2 + (D + 1) * BLOCK_M + r) > 0.f)) continue;
+                    const float w2 = ex2_approx(__ldcg(b2 + D * BLOCK_M + r) - M);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __float_as_uint(fmaf(w2, __ldcg(b2 + (c * 32 + i) * BLOCK_M + r), __uint_as_float(o[i])));
                 }
                 if (store) {
                     if constexpr (OUT_BF16) {
@@ -507,15 +658,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + obase + c * 32);
 #pragma unroll
                         for (int v4 = 0; v4 < 8; ++v4)
-                            dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
-                                                  __uint_as_float(o[4 * v4 + 2]) * inv,
-                                                  __uint_as_float(o[4 * v4 + 3]) * inv);
+                            dst[v4] = make_float4(
+                                __uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
+                                __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
                     }
                 }
             }
             if (store && p.LSE) {
-                const float lse = (have && l_run > 0.f) ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
-                p.LSE[static_cast<size_t>(bh) * p.N + row] = lse;
+                const float lse = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+                p.LSE[static_cast<size_t>(bh) * p.plan.N + row] = lse;
             }
         }
     }
@@ -533,8 +684,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // V -> fp16 with a per-head power-of-two scale: pass 1 takes |V| maxima per chunk, pass 2 picks
 // the head's exponent e (so that |V| * 2^-e < 2^15) and writes V * 2^-e rounded to fp16.
 // ---------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) vprep_absmax_kernel(const VPrepParams p) {
+// The schedule's batch offsets: boff[b] = sum over b' < b of H * (one head's cost in batch b'),
+// computed by one block; it also clears the partial-result flags of the attention kernel.
+__device__ void plan_block(const PlanParams& pl) {
+    __shared__ long long part[256];
+    const int tid = threadIdx.x;
+    const int per = (pl.B + 255) / 256;
+    const int b0 = min(pl.B, tid * per), b1 = min(pl.B, b0 + per);
+    long long sum = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int nb = key_tiles(clamp_len(pl.kv_len, b, pl.N));
+        sum += static_cast<long long>(pl.H) * pair_prefix(pl.n_pairs, nb, pl.N, pl.causal);
+    }
+    part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {  // exclusive scan of 256 partial sums
+        long long run = 0;
+        for (int i = 0; i < 256; ++i) {
+            const long long v = part[i];
+            part[i] = run;
+            run += v;
+        }
+        pl.boff[pl.B] = run;
+    }
+    __syncthreads();
+    long long run = part[tid];
+    for (int b = b0; b < b1; ++b) {
+        pl.boff[b] = run;
+        const int nb = key_tiles(clamp_len(pl.kv_len, b, pl.N));
+        run += static_cast<long long>(pl.H) * pair_prefix(pl.n_pairs, nb, pl.N, pl.causal);
+    }
+    for (int i = tid; i < 8 * SCHED_MAX_CTAS; i += 256) pl.flags[i] = 0u;
+}
+
+__global__ void __launch_bounds__(256) vprep_absmax_kernel(const VPrepParams p, const PlanParams pl) {
     const int chunk = blockIdx.x, head = blockIdx.y;
+    if (head == p.heads) {  // the extra row of blocks: block 0 plans, the others have nothing to do
+        if (chunk == 0) plan_block(pl);
+        return;
+    }
     const long long base = static_cast<long long>(head) * p.elems_per_head + static_cast<long long>(chunk) * VPREP_CHUNK;
     const long long end = min(base + VPREP_CHUNK, static_cast<long long>(head + 1) * p.elems_per_head);
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.V) + base);
@@ -599,12 +787,11 @@ __global__ void __launch_bounds__(256) vprep_convert_kernel(const VPrepParams p)
     }
 }
 
-cudaError_t launch_vprep(const VPrepParams& p, cudaStream_t stream) {
-    dim3 grid(p.chunks, p.heads);
-    vprep_absmax_kernel<<<grid, 256, 0, stream>>>(p);
+cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStream_t stream) {
+    vprep_absmax_kernel<<<dim3(p.chunks, p.heads + 1), 256, 0, stream>>>(p, plan);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    vprep_convert_kernel<<<grid, 256, 0, stream>>>(p);
+    vprep_convert_kernel<<<dim3(p.chunks, p.heads), 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -620,9 +807,21 @@ static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, c
     e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidKernelImage;
-    const long long grid = static_cast<long long>(p.n_pairs) * p.B * p.H;
-    if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
+    if (p.plan.G <= 0 || p.plan.G > SCHED_MAX_CTAS) return cudaErrorInvalidConfiguration;
+    // Cooperative launch: every CTA is resident at once, so an owner CTA may wait (bounded) for the
+    // partial results of the CTAs after it.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.plan.G));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = Cfg<D>::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -641,6 +840,36 @@ extern "C" int attn_debug_read_trace(long long* host, int n) {
     return cudaMemcpyFromSymbol(host, g_attn_trace, sizeof(g_attn_trace)) == cudaSuccess ? 0 : -1;
 }
 #endif
+
+// Line length of the worst case (every kv_len = N): the schedule needs it below 2^31.
+long long plan_max_steps(int B, int H, int N, int causal) {
+    const int n_pairs = (N + 2 * BLOCK_M - 1) / (2 * BLOCK_M);
+    return static_cast<long long>(B) * H * pair_prefix(n_pairs, key_tiles(N), N, causal);
+}
+
+SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms) {
+    SchedPlan p{};
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.causal = causal;
+    p.n_pairs = (N + 2 * BLOCK_M - 1) / (2 * BLOCK_M);
+    const long long units = static_cast<long long>(B) * H * p.n_pairs;
+    const int nb = key_tiles(N);
+    const long long w_max = static_cast<long long>(B) * H * pair_prefix(p.n_pairs, nb, N, causal);
+    long long g = sms < SCHED_MAX_CTAS ? sms : SCHED_MAX_CTAS;
+    const long long g_steps = (w_max + SCHED_MIN_STEPS - 1) / SCHED_MIN_STEPS;
+    if (g_steps < g) g = g_steps;
+    if (g < 1) g = 1;
+    p.G = static_cast<int>(g);
+    // data-parallel rounds only when every unit costs the same; the last one or two rounds' worth of
+    // units go to the balanced stream-K part
+    const bool uniform = !causal && !has_kv_len;
+    const long long r = uniform ? units / g - 1 : 0;
+    p.R_dp = r > 0 ? static_cast<int>(r) : 0;
+    p.S0 = static_cast<int>(static_cast<long long>(p.R_dp) * p.G * nb);
+    return p;
+}
 
 cudaError_t read_and_clear_error(uint32_t* out, cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);

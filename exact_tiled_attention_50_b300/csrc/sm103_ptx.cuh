@@ -271,6 +271,36 @@ __device__ __forceinline__ void regs_decrease() {
 }
 
 // ---------------------------------------------------------------------------------------------
+// Flags between CTAs of one (cooperative) launch
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void flag_release(unsigned int* f, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int flag_acquire(const unsigned int* f) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+
+// Wait until *f == v; false if the limit (SM cycles, as in mbar_wait) ran out or *abort was set.
+__device__ __forceinline__ bool flag_wait(const unsigned int* f, unsigned int v, uint64_t limit_ns,
+                                          const volatile int* abort) {
+    if (flag_acquire(f) == v) return true;
+    const long long t0 = clock64();
+    const long long limit_cycles = static_cast<long long>(limit_ns) * 2;
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i) {
+            __nanosleep(64);
+            if (flag_acquire(f) == v) return true;
+        }
+        if (*abort) return false;
+        if (clock64() - t0 > limit_cycles) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
 // Misc
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {

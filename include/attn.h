@@ -95,10 +95,18 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
  */
 attn_status attn_check(cudaStream_t stream);
 
+/*
+ * Diagnostic detail of the last attn_check on this process: 0, or the device error bits it read
+ * (bit 0: a bounded wait ran out; higher bits name the wait: 2 Q tile, 4 key/value stage, 8 scores,
+ * 16 probabilities, 32 output, 64 free stage, 128 final drain, 256 another CTA's partial result).
+ */
+uint32_t attn_debug_last_error_bits(void);
+
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status s);
 
-/* Number of kernel launches attn_fwd enqueues for these arguments (1 for fp32, 3 for bf16). */
+/* Number of kernel launches attn_fwd enqueues for these arguments (1 for fp32, 3 for bf16: the V
+ * pre-pass with the schedule plan, the V conversion and the persistent attention kernel). */
 int attn_launches_per_call(attn_dtype in_dtype);
 
 /*
@@ -111,6 +119,17 @@ int attn_launches_per_call(attn_dtype in_dtype);
  */
 void attn_debug_set_wait_limit_ns(uint64_t ns);
 void attn_debug_set_skip_kv_load(int on);
+
+/*
+ * Test hook (host only, no GPU needed): the work schedule the tensor-core kernel would follow for
+ * these sizes on a device with `sms` SMs, with kv_len given as a HOST int32 array [B] (or NULL).
+ * Writes up to max_segments records (out may be NULL when max_segments is 0) of 8 int32 (cta, b, h, pair, k0, k1, cost, kind; kind 0 = the
+ * whole unit, 1 = the piece that holds the unit's first key step and merges the others, 2 = a later
+ * piece that hands its partial result to that one) in the order each CTA runs them, and returns the
+ * total number of segments (-1 on invalid arguments).
+ */
+int attn_debug_schedule(int B, int H, int N, int causal, const int32_t* kv_len_host, int sms, int32_t* out,
+                        int max_segments);
 
 /*
  * Timing hook for benchmarks: while set (both non-NULL), every attn_fwd call records `start` on its

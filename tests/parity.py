@@ -22,7 +22,7 @@ def run_gpu(x, out_dtype=torch.float32, device="cuda"):
     kv = x.kv_len.to(device) if x.kv_len is not None else None
     O, L = attn.attn_fwd(q, k, v, scale=x.scale, causal=x.causal, kv_len=kv, out_dtype=out_dtype)
     rc = attn.check()
-    assert rc == attn.ATTN_OK, attn.status_string(rc)
+    assert rc == attn.ATTN_OK, f"{attn.status_string(rc)} bits {attn.lib.attn_debug_last_error_bits():#x}"
     return O, L
 
 
