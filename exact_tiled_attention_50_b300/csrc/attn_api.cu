@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <atomic>
 #include <mutex>
@@ -90,6 +91,19 @@ bool encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, i
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map over the fp32 output [slabs, rows, d]: box of 32 columns x 32 rows, 128-byte swizzle
+// (the layout the epilogue stages rows in); rows past `rows` are not written by stores.
+bool encode_out_map(CUtensorMap* m, void* base, int d, int rows, long long slabs) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(slabs)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(rows) * d * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool sizes_ok(int B, int H, int H_kv, int N, int d) {
     if (B <= 0 || H <= 0 || H_kv <= 0 || N <= 0) return false;
     if (H % H_kv != 0) return false;
@@ -160,6 +174,9 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
         !encode_rows_map(&tmK, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, N, static_cast<long long>(B) * H_kv) ||
         !encode_rows_map(&tmV, vp.V16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, d, N, static_cast<long long>(B) * H_kv))
         return ATTN_ERR_UNSUPPORTED;
+    CUtensorMap tmO;
+    memset(&tmO, 0, sizeof(tmO));
+    if (out_dtype == ATTN_F32 && !encode_out_map(&tmO, O, d, N, static_cast<long long>(B) * H)) return ATTN_ERR_UNSUPPORTED;
 
     const int sms = device_sms();
     if (sms <= 0) return ATTN_ERR_CUDA;
@@ -188,7 +205,7 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
     const bool timed = ev0 && ev1;
     if (timed && cudaEventRecord(ev0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (attn_impl::launch_attn_tc(d, out_dtype == ATTN_BF16, tmQ, tmK, tmV, p, stream) != cudaSuccess)
+    if (attn_impl::launch_attn_tc(d, out_dtype == ATTN_BF16, tmQ, tmK, tmV, tmO, p, stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
     if (timed && cudaEventRecord(ev1, stream) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;

@@ -231,8 +231,9 @@ struct VPrepParams {
 constexpr int VPREP_CHUNK = 16384;  // elements of V per CTA in the fp16 conversion
 
 cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStream_t stream);
+// tmO: fp32 output map (box 32 columns x 32 rows, 128-byte swizzle); unused for bf16 output.
 cudaError_t launch_attn_tc(int d, bool out_bf16, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV16, const TcParams& p, cudaStream_t stream);
+                           const CUtensorMap& tmV16, const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream);
 
 // Persistent-CTA plan for these sizes on a device with `sms` SMs (kv_len given or not).
 SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms);

@@ -45,8 +45,9 @@ using namespace attn_sm103;
 
 __device__ unsigned int g_attn_error = 0;
 
-// Optional timeline trace (builds with -DATTN_TRACE only): clock64 stamps of CTA 0's MMA warp and
-// of thread 0 of each softmax warpgroup, per key tile, for profiling the pipeline by hand.
+// Optional timeline trace (builds with -DATTN_TRACE only): clock64 stamps of CTA 0's MMA warp (per
+// ring step) and of thread 0 of each softmax warpgroup (per key step of its tile), for profiling the
+// pipeline by hand.
 #ifdef ATTN_TRACE
 constexpr int TRACE_J = 128, TRACE_EV = 8;
 __device__ long long g_attn_trace[3][TRACE_J][TRACE_EV];
@@ -54,7 +55,17 @@ __device__ long long g_attn_trace[3][TRACE_J][TRACE_EV];
     do {                                                                             \
         if (blockIdx.x == 0 && (j) < TRACE_J) g_attn_trace[role][j][ev] = clock64(); \
     } while (0)
+// per CTA and segment: global-timer stamps (ns) of segment events, for the whole grid
+constexpr int TRACE_CTAS = 160, TRACE_SEGS = 16, TRACE_SEG_EV = 8;
+__device__ long long g_attn_seg_trace[TRACE_CTAS][TRACE_SEGS][TRACE_SEG_EV];
+#define ATTN_SEG_TRACE(seg, ev, val)                                                          \
+    do {                                                                                      \
+        if (blockIdx.x < TRACE_CTAS && (seg) < TRACE_SEGS) g_attn_seg_trace[blockIdx.x][seg][ev] = (val); \
+    } while (0)
 #else
+#define ATTN_SEG_TRACE(seg, ev, val) \
+    do {                             \
+    } while (0)
 #define ATTN_TRACE_AT(role, j, ev) \
     do {                           \
     } while (0)
@@ -93,6 +104,9 @@ struct Cfg {
     static constexpr uint32_t IDESC_S = idesc_f16(BLOCK_M, BLOCK_N, 1, 1, 0, 0);  // bf16, K-major both
     static constexpr uint32_t IDESC_O = idesc_f16(BLOCK_M, D, 0, 0, 0, 1);        // f16, B (V) MN-major
     static constexpr uint32_t TMEM_O = 256;
+    // epilogue staging buffers (4 KB each) per softmax warp inside its tile's Q region
+    static constexpr int EPI_BUFS = TILE_BYTES / 4 / 4096;
+    static_assert(EPI_BUFS >= 1, "staging");
 };
 
 __device__ __forceinline__ void record_failure(volatile int* abort_flag, uint32_t bits) {
@@ -148,7 +162,8 @@ __device__ __forceinline__ SegInfo seg_info(const TcParams& p, const Segment& s)
 template <int D, bool OUT_BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ TcParams p) {
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                       const __grid_constant__ TcParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -160,6 +175,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __shared__ __align__(8) uint64_t bar_s_full[2];         // S_t in TMEM
     __shared__ __align__(8) uint64_t bar_p_full[2][2];      // half h of P_t in TMEM (O_t rescaled)
     __shared__ __align__(8) uint64_t bar_o_full[2];         // last P V of the segment into O_t done
+    __shared__ __align__(8) uint64_t bar_q_free[2];         // Q_t's shared memory no longer used by the epilogue
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
@@ -198,6 +214,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&bar_p_full[t][0], 128);
             mbar_init(&bar_p_full[t][1], 128);
             mbar_init(&bar_o_full[t], 1);
+            mbar_init(&bar_q_free[t], 4);
         }
         mbar_init(&bar_drain, 1);
         abort_flag = 0;
@@ -205,6 +222,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        if (!OUT_BF16) tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
     __syncthreads();
@@ -230,7 +248,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 while (ok && walk_next(walk, tab, p.plan, static_cast<int>(blockIdx.x), seg_sh[TMA_WARP])) {
                     const SegInfo si = seg_info(p, s);
                     if (si.nmax == 0) continue;
-                    if (segq > 0 && !mbar_wait(&bar_q_empty, (segq - 1) & 1, limit_ns, &abort_flag)) {
+                    // Q_t and the first-K region are reused once the previous segment's MMAs completed
+                    // and (Q_t) its epilogue finished staging output rows there
+                    if (segq > 0 && (!mbar_wait(&bar_q_empty, (segq - 1) & 1, limit_ns, &abort_flag) ||
+                                     !mbar_wait(&bar_q_free[0], (segq - 1) & 1, limit_ns, &abort_flag) ||
+                                     !mbar_wait(&bar_q_free[1], (segq - 1) & 1, limit_ns, &abort_flag))) {
                         record_failure(&abort_flag, ERRBIT_WAIT_EMPTY);
                         ok = false;
                         break;
@@ -321,13 +343,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t g = 0, segq = 0;
             uint32_t cnt_p[2] = {0u, 0u};
             bool ok = true;
+            int seg_no = -1;  // trace index
             while (ok && next_seg()) {
+                ++seg_no;
                 const SegInfo si = seg_info(p, s);
+                if (lane == 0) ATTN_SEG_TRACE(seg_no, 0, static_cast<long long>(global_timer_ns()));
+                if (lane == 0) ATTN_SEG_TRACE(seg_no, 6, s.kind * 1000000LL + (s.k1 - s.k0));
                 if (si.nmax == 0) continue;
                 if (!wait_all(&bar_q, segq & 1, ERRBIT_WAIT_Q)) {
                     ok = false;
                     break;
                 }
+                if (lane == 0) ATTN_SEG_TRACE(seg_no, 1, static_cast<long long>(global_timer_ns()));
                 ++segq;
                 tc_fence_after();
                 if (elect_one()) {
@@ -388,6 +415,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // Q and the first K of this segment may be overwritten once these MMAs completed
                 if (elect_one()) umma_commit(&bar_q_empty);
                 __syncwarp();
+                if (lane == 0) ATTN_SEG_TRACE(seg_no, 2, static_cast<long long>(global_timer_ns()));
             }
             // Drain: every MMA this warp issued has completed before tensor memory is freed.
             if (elect_one()) umma_commit(&bar_drain);
@@ -409,10 +437,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool trace_me = (threadIdx.x & 127) == 0;
         const int G = p.plan.G;
         const Segment& s = seg_sh[warp];
-        uint32_t cnt_s = 0, cnt_o = 0;
+        uint32_t cnt_s = 0, cnt_o = 0;  // cnt_s also numbers this tile's key steps (trace index)
+        uint32_t segq = 0;              // segments whose Q the producer loaded (as it counts them)
         bool ok = true;
+        int seg_no = -1;  // trace index
 
         while (ok && next_seg()) {
+            ++seg_no;
+            // In a segment whose Q the producer loads, this warpgroup may hand Q_t's shared memory
+            // back (bar_q_free) only after that load landed: the producer then waits for exactly one
+            // outstanding q_free phase per tile, even for a tile without keys in the segment.
+            if (seg_info(p, s).nmax > 0) {
+                const bool got = mbar_wait(&bar_q, segq & 1, limit_ns, &abort_flag);
+                ++segq;
+                if (!__all_sync(0xffffffffu, got)) {
+                    if (!got) record_failure(&abort_flag, ERRBIT_WAIT_Q);
+                    ok = false;
+                    break;
+                }
+            }
             // only what the key loop needs stays in registers; the rest is re-read from shared memory
             const int k0 = s.k0;
             const int q0t = s.pair * 2 * BLOCK_M + t * BLOCK_M;
@@ -422,6 +465,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int hi = min(s.k1, key_tiles(p.plan.causal ? min(kv_valid, q0t + BLOCK_M) : kv_valid));
                 nkvt = hi > k0 ? hi - k0 : 0;
             }
+
             const int row = q0t + r;                   // query index
             const int row_lim = p.plan.causal ? min(kv_valid, row + 1) : kv_valid;  // keys < row_lim are valid
             float m_run = -INFINITY;                   // reference maximum (log2 domain, already scaled)
@@ -431,7 +475,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int j = k0 + jj;
                 // tcgen05.ld/st below are warp-collective: the warp proceeds only if every lane's wait
                 // succeeded
-                if (trace_me) ATTN_TRACE_AT(1 + t, j, 0);
+                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s, 0);
                 const bool got = mbar_wait(&bar_s_full[t], cnt_s & 1, limit_ns, &abort_flag);
                 ++cnt_s;
                 if (!__all_sync(0xffffffffu, got)) {
@@ -440,7 +484,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                if (trace_me) ATTN_TRACE_AT(1 + t, j, 1);
+                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 1);
                 uint32_t ra[32], rb[32], rc[32], rd[32];
                 tmem_ld32(tS + 0, ra);
                 tmem_ld32(tS + 32, rb);
@@ -450,7 +494,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_wait_ld(rb);
                 tmem_wait_ld(rc);
                 tmem_wait_ld(rd);
-                if (trace_me) ATTN_TRACE_AT(1 + t, j, 2);
+                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 2);
                 float x[128];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -507,7 +551,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tmem_st32(tO + c * 32, o);
                     }
                 }
-                if (trace_me) ATTN_TRACE_AT(1 + t, j, 3);
+                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 3);
                 const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
                 // P = exp2(s * scale*log2e - m), written to TMEM as fp16 pairs over the first 64 columns
                 // of S_t, one half (64 keys) at a time; each half is announced as soon as it is stored.
@@ -536,14 +580,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tmem_wait_st();
                         tc_fence_before();
                         mbar_arrive(&bar_p_full[t][half]);
-                        if (trace_me) ATTN_TRACE_AT(1 + t, j, 4 + half);
+                        if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 4 + half);
                     }
                     float s0, s1, s2, s3;
                     split_f32x2(acc0, s0, s1);
                     split_f32x2(acc1, s2, s3);
                     l_run += (s0 + s1) + (s2 + s3);
                 }
-                if (trace_me) ATTN_TRACE_AT(1 + t, j, 6);
+                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 6);
             }
             if (!ok) break;
 
@@ -560,6 +604,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
             }
             const bool live = have && l_run > 0.f;     // this row got weight from this piece
+            // the producer loads Q (and waits for this warpgroup's q_free) only for segments with keys
+            const bool seg_loads_q = seg_info(p, s).nmax > 0;
+            if ((threadIdx.x & 127) == 0) ATTN_SEG_TRACE(seg_no, 3 + t, static_cast<long long>(global_timer_ns()));
 
             if (s.kind == SEG_WRITER) {
                 // partial result for the owner of the unit: unnormalised O (row fastest), m, l
@@ -578,10 +625,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 base[(D + 1) * BLOCK_M + r] = live ? l_run : 0.f;
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) flag_release(p.flags + (blockIdx.x * 2 + t) * 4 + wq, 1u);
+                if (lane == 0) {
+                    flag_release(p.flags + (blockIdx.x * 2 + t) * 4 + wq, 1u);
+                    if (seg_loads_q) mbar_arrive(&bar_q_free[t]);
+                }
                 continue;
             }
-            if (q0t >= p.plan.N) continue;              // a tile past the last row: nothing to write
+            if (q0t >= p.plan.N) {                      // a tile past the last row: nothing to write
+                if (lane == 0 && seg_loads_q) mbar_arrive(&bar_q_free[t]);
+                continue;
+            }
 
             // COMPLETE or OWNER: gather the partial results of the unit's other pieces (owner only)
             const int W = walk_sh[warp].W;
@@ -618,6 +671,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float inv = L > 0.f ? vscale / L : 0.f;
             const bool store = row < p.plan.N;
             const size_t obase = (static_cast<size_t>(bh) * p.plan.N + (store ? row : 0)) * D;
+            const uint32_t stage_base = smem_u32(smem + t * C::TILE_BYTES + wq * C::EPI_BUFS * 4096);
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -640,8 +694,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int i = 0; i < 32; ++i)
                         o[i] = __float_as_uint(fmaf(w2, __ldcg(b2 + (c * 32 + i) * BLOCK_M + r), __uint_as_float(o[i])));
                 }
-                if (store) {
-                    if constexpr (OUT_BF16) {
+                if (OUT_BF16 || !seg_loads_q) {
+                    if (store && OUT_BF16) {
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + obase + c * 32);
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4) {
@@ -654,7 +708,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                             dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                    } else {
+                    } else if (store) {
+                        // (a unit without keys: no staging, its Q region may be in use by the producer)
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + obase + c * 32);
 #pragma unroll
                         for (int v4 = 0; v4 < 8; ++v4)
@@ -662,16 +717,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 __uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
                                 __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
                     }
+                } else {
+                    // fp32 rows leave through the tensor store engine: the warp stages its 32 rows x 32
+                    // columns (128-byte swizzled, 4 KB) in Q_t's shared memory, free since every S_t
+                    // MMA of the segment completed, and one lane stores the box (rows past N are not
+                    // written). Buffers are reused once the store engine has read them.
+                    const uint32_t buf = stage_base + (c % C::EPI_BUFS) * 4096;
+                    if (c >= C::EPI_BUFS) {
+                        if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        st_shared_v4(buf + lane * 128 + ((k ^ (lane & 7)) << 4),
+                                     __float_as_uint(__uint_as_float(o[4 * k]) * inv),
+                                     __float_as_uint(__uint_as_float(o[4 * k + 1]) * inv),
+                                     __float_as_uint(__uint_as_float(o[4 * k + 2]) * inv),
+                                     __float_as_uint(__uint_as_float(o[4 * k + 3]) * inv));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tmO, smem + (buf - smem_u32(smem)), c * 32, q0t + wq * 32, bh);
+                        bulk_commit_group();
+                    }
+                    __syncwarp();
                 }
             }
             if (store && p.LSE) {
                 const float lse = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
                 p.LSE[static_cast<size_t>(bh) * p.plan.N + row] = lse;
             }
+            if (lane == 0 && seg_loads_q) {
+                if (!OUT_BF16) bulk_wait_group_read<0>();  // the staging buffers may be overwritten
+                mbar_arrive(&bar_q_free[t]);
+            }
+            if ((threadIdx.x & 127) == 0) ATTN_SEG_TRACE(seg_no, 5 + 2 * t, static_cast<long long>(global_timer_ns()));
         }
     }
 
     // ---- teardown ----
+    if (!OUT_BF16 && warp < 8 && lane == 0) bulk_wait_group_all();  // output stores performed
     tc_fence_before();
     __syncthreads();
     if (warp == MMA_WARP) {
@@ -797,7 +882,7 @@ cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStrea
 
 template <int D, bool OUT_BF16>
 static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                               const TcParams& p, cudaStream_t stream) {
+                               const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
     auto kern = attn_fwd_tc_kernel<D, OUT_BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -820,17 +905,17 @@ static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, c
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, tmO, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t launch_attn_tc(int d, bool out_bf16, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV16, const TcParams& p, cudaStream_t stream) {
-    if (d == 128) return out_bf16 ? launch_tc_t<128, true>(tmQ, tmK, tmV16, p, stream)
-                                  : launch_tc_t<128, false>(tmQ, tmK, tmV16, p, stream);
-    if (d == 64) return out_bf16 ? launch_tc_t<64, true>(tmQ, tmK, tmV16, p, stream)
-                                 : launch_tc_t<64, false>(tmQ, tmK, tmV16, p, stream);
+                           const CUtensorMap& tmV16, const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
+    if (d == 128) return out_bf16 ? launch_tc_t<128, true>(tmQ, tmK, tmV16, tmO, p, stream)
+                                  : launch_tc_t<128, false>(tmQ, tmK, tmV16, tmO, p, stream);
+    if (d == 64) return out_bf16 ? launch_tc_t<64, true>(tmQ, tmK, tmV16, tmO, p, stream)
+                                 : launch_tc_t<64, false>(tmQ, tmK, tmV16, tmO, p, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -838,6 +923,11 @@ cudaError_t launch_attn_tc(int d, bool out_bf16, const CUtensorMap& tmQ, const C
 extern "C" int attn_debug_read_trace(long long* host, int n) {
     if (n < 3 * TRACE_J * TRACE_EV) return -1;
     return cudaMemcpyFromSymbol(host, g_attn_trace, sizeof(g_attn_trace)) == cudaSuccess ? 0 : -1;
+}
+
+extern "C" int attn_debug_read_seg_trace(long long* host, int n) {
+    if (n < TRACE_CTAS * TRACE_SEGS * TRACE_SEG_EV) return -1;
+    return cudaMemcpyFromSymbol(host, g_attn_seg_trace, sizeof(g_attn_seg_trace)) == cudaSuccess ? 0 : -1;
 }
 #endif
 
