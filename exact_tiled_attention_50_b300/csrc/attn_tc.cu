@@ -14,8 +14,9 @@
 //   warps 0-3  softmax warpgroup for query tile 0 (rows 0-127 of the CTA's 256 rows)
 //   warps 4-7  softmax warpgroup for query tile 1 (rows 128-255)
 //   warp  8    tensor-memory owner and MMA issuer (converged warp; one elected lane issues)
-//   warp  9    TMA producer (Q_0, Q_1 and K_0 once, then a ring of (V_j, K_j+1) stages)
-//   warps 10-11 idle (they complete the third warpgroup for the register split)
+//   warp  9    TMA producer of the key/value tiles (K_k0 per segment, then a ring of (V_j, K_j+1))
+//   warp 10    TMA producer of the query tiles Q_0, Q_1 (once per segment)
+//   warp 11    idle (it completes the third warpgroup for the register split)
 // Tensor memory (512 columns x 128 lanes x 32 bit): S_0 [0,128), S_1 [128,256), O_0 and O_1 after
 // that (d columns each). P_t (fp16, two per column) overwrites the first 64 columns of S_t after the
 // softmax has read S_t into registers; the P V MMA reads P straight from tensor memory.
@@ -77,7 +78,8 @@ constexpr int BLOCK_M = 128;              // query rows per tile (tcgen05 M)
 constexpr int BLOCK_N = 128;              // keys per tile
 constexpr int NUM_THREADS = 384;          // 3 warpgroups
 constexpr int MMA_WARP = 8;
-constexpr int TMA_WARP = 9;
+constexpr int TMA_WARP = 9;                // key/value ring producer
+constexpr int QLOAD_WARP = 10;             // query tile producer
 // Lazy rescale: a row keeps its reference maximum until a tile's maximum exceeds it by more than
 // 2^15 (log2 units); exponentials then stay <= 2^15, inside the fp16 range of P (65504).
 constexpr float RESCALE_THRESHOLD = 15.0f;
@@ -95,7 +97,8 @@ template <int D>
 struct Cfg {
     static constexpr int NB = D / 64;                 // 64-element (128-byte) boxes per row
     static constexpr int TILE_BYTES = NB * 16384;     // one 128 x D tile of 16-bit values
-    // Shared memory: Q_0, Q_1, K_0, then NP ring stages of (V_j, K_j+1), consumed together.
+    // Shared memory: Q_0, Q_1, the segment's first key tile K_k0, then NP ring stages of
+    // (V_j, K_j+1), consumed together (one wait and one release per key step).
     static constexpr int NP = (D == 128) ? 2 : 4;
     static constexpr int OFF_K0 = 2 * TILE_BYTES;
     static constexpr int OFF_RING = 3 * TILE_BYTES;
@@ -168,8 +171,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    __shared__ __align__(8) uint64_t bar_q;                 // Q_0, Q_1 and the segment's first K landed
+    __shared__ __align__(8) uint64_t bar_q;                 // the segment's Q_0, Q_1 landed
     __shared__ __align__(8) uint64_t bar_q_empty;           // every MMA of the segment completed
+    __shared__ __align__(8) uint64_t bar_k0_full;           // the segment's first K tile landed
+    __shared__ __align__(8) uint64_t bar_k0_empty;          // the segment's first S MMAs completed
     __shared__ __align__(8) uint64_t bar_full[C::NP];       // ring stage (V_j, K_j+1) landed
     __shared__ __align__(8) uint64_t bar_empty[C::NP];      // ring stage free again
     __shared__ __align__(8) uint64_t bar_s_full[2];         // S_t in TMEM
@@ -179,15 +184,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
-    // Work-schedule walkers, one per working warp (warps 0-9), advanced by one lane; the current
+    // Work-schedule walkers, one per working warp (warps 0-10), advanced by one lane; the current
     // segment is read from shared memory so that the walker state stays out of registers.
-    __shared__ WalkState walk_sh[10];
-    __shared__ Segment seg_sh[10];
+    __shared__ WalkState walk_sh[11];
+    __shared__ Segment seg_sh[11];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const DevSchedTab tab{p};
-    if (warp < 10 && lane == 0) walk_init(walk_sh[warp], tab, p.plan);
+    if (warp < 11 && lane == 0) walk_init(walk_sh[warp], tab, p.plan);
     // warp-collective: the next segment of this warp's walker into seg_sh[warp]
     auto next_seg = [&]() -> bool {
         int more = 0;
@@ -205,6 +210,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == TMA_WARP * 32) {
         mbar_init(&bar_q, 1);
         mbar_init(&bar_q_empty, 1);
+        mbar_init(&bar_k0_full, 1);
+        mbar_init(&bar_k0_empty, 1);
         for (int s = 0; s < C::NP; ++s) {
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_empty[s], 1);
@@ -235,44 +242,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp >= 8) {
         regs_decrease<CONTROL_REGS>();
         if (warp == TMA_WARP) {
-            // ============================== TMA producer (one lane) ==============================
+            // ============ key/value producer (one lane): K_k0 per segment, then the stage ring ============
             if (elect_one()) {
                 const uint64_t pol_kv = l2_policy_evict_last();
-                const uint64_t pol_q = l2_policy_evict_first();
                 WalkState& walk = walk_sh[TMA_WARP];
                 const Segment& s = seg_sh[TMA_WARP];
                 uint32_t g = 0;        // ring steps issued
-                uint32_t segq = 0;     // segments whose Q was issued
+                uint32_t segk = 0;     // segments whose first K was issued
                 bool ok = true;
                 bool skip_k = p.debug_skip_kv_load != 0;  // failure-path test: the first K is never loaded
                 while (ok && walk_next(walk, tab, p.plan, static_cast<int>(blockIdx.x), seg_sh[TMA_WARP])) {
                     const SegInfo si = seg_info(p, s);
                     if (si.nmax == 0) continue;
-                    // Q_t and the first-K region are reused once the previous segment's MMAs completed
-                    // and (Q_t) its epilogue finished staging output rows there
-                    if (segq > 0 && (!mbar_wait(&bar_q_empty, (segq - 1) & 1, limit_ns, &abort_flag) ||
-                                     !mbar_wait(&bar_q_free[0], (segq - 1) & 1, limit_ns, &abort_flag) ||
-                                     !mbar_wait(&bar_q_free[1], (segq - 1) & 1, limit_ns, &abort_flag))) {
+                    if (segk > 0 && !mbar_wait(&bar_k0_empty, (segk - 1) & 1, limit_ns, &abort_flag)) {
                         record_failure(&abort_flag, ERRBIT_WAIT_EMPTY);
                         ok = false;
                         break;
                     }
-                    uint32_t qbytes = C::TILE_BYTES;  // the segment's first K tile
-                    qbytes += si.n[0] > 0 ? C::TILE_BYTES : 0;
-                    qbytes += si.n[1] > 0 ? C::TILE_BYTES : 0;
-                    mbar_arrive_expect_tx(&bar_q, qbytes);
-#pragma unroll
-                    for (int t = 0; t < 2; ++t)
-                        if (si.n[t] > 0)
-                            for (int bx = 0; bx < C::NB; ++bx)
-                                tma_load_3d_hint(smem + t * C::TILE_BYTES + bx * 16384, &tmQ, &bar_q, bx * 64,
-                                                 si.q0[t], si.bh, pol_q);
+                    mbar_arrive_expect_tx(&bar_k0_full, C::TILE_BYTES);
                     if (!skip_k)
                         for (int bx = 0; bx < C::NB; ++bx)
-                            tma_load_3d_hint(smem + C::OFF_K0 + bx * 16384, &tmK, &bar_q, bx * 64, s.k0 * BLOCK_N,
-                                             si.zkv, pol_kv);
+                            tma_load_3d_hint(smem + C::OFF_K0 + bx * 16384, &tmK, &bar_k0_full, bx * 64,
+                                             s.k0 * BLOCK_N, si.zkv, pol_kv);
                     skip_k = false;
-                    ++segq;
+                    ++segk;
                     const int jend = s.k0 + si.nmax;
                     for (int j = s.k0; j < jend; ++j) {
                         const uint32_t st = g % C::NP;
@@ -299,9 +292,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // lands in shared memory after the CTA has exited.
                 if (!ok || abort_flag) {
                     volatile int never = 0;  // these waits must not be cut short by the abort flag
-                    if (segq > 0) (void)mbar_wait(&bar_q, (segq - 1) & 1, limit_ns, &never);
+                    if (segk > 0) (void)mbar_wait(&bar_k0_full, (segk - 1) & 1, limit_ns, &never);
                     for (uint32_t gg = g > C::NP ? g - C::NP : 0; gg < g; ++gg)
                         (void)mbar_wait(&bar_full[gg % C::NP], (gg / C::NP) & 1, limit_ns, &never);
+                }
+            }
+            __syncwarp();
+        } else if (warp == QLOAD_WARP) {
+            // ====================== query producer (one lane): Q_0, Q_1 per segment ======================
+            if (elect_one()) {
+                const uint64_t pol_q = l2_policy_evict_first();
+                WalkState& walk = walk_sh[QLOAD_WARP];
+                const Segment& s = seg_sh[QLOAD_WARP];
+                uint32_t segq = 0;     // segments whose Q was issued
+                bool ok = true;
+                while (ok && walk_next(walk, tab, p.plan, static_cast<int>(blockIdx.x), seg_sh[QLOAD_WARP])) {
+                    const SegInfo si = seg_info(p, s);
+                    if (si.nmax == 0) continue;
+                    // Q_t is reused once the previous segment's MMAs completed and its epilogue
+                    // finished staging output rows there
+                    if (segq > 0 && (!mbar_wait(&bar_q_empty, (segq - 1) & 1, limit_ns, &abort_flag) ||
+                                     !mbar_wait(&bar_q_free[0], (segq - 1) & 1, limit_ns, &abort_flag) ||
+                                     !mbar_wait(&bar_q_free[1], (segq - 1) & 1, limit_ns, &abort_flag))) {
+                        record_failure(&abort_flag, ERRBIT_WAIT_EMPTY);
+                        ok = false;
+                        break;
+                    }
+                    uint32_t qbytes = 0;
+                    qbytes += si.n[0] > 0 ? C::TILE_BYTES : 0;
+                    qbytes += si.n[1] > 0 ? C::TILE_BYTES : 0;
+                    mbar_arrive_expect_tx(&bar_q, qbytes);
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+                        if (si.n[t] > 0)
+                            for (int bx = 0; bx < C::NB; ++bx)
+                                tma_load_3d_hint(smem + t * C::TILE_BYTES + bx * 16384, &tmQ, &bar_q, bx * 64,
+                                                 si.q0[t], si.bh, pol_q);
+                    ++segq;
+                }
+                if (!ok || abort_flag) {
+                    volatile int never = 0;
+                    if (segq > 0) (void)mbar_wait(&bar_q, (segq - 1) & 1, limit_ns, &never);
                 }
             }
             __syncwarp();
@@ -340,7 +371,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             };
             const Segment& s = seg_sh[MMA_WARP];
-            uint32_t g = 0, segq = 0;
+            uint32_t g = 0, segq = 0;    // ring steps consumed, segments with a Q load
             uint32_t cnt_p[2] = {0u, 0u};
             bool ok = true;
             int seg_no = -1;  // trace index
@@ -350,12 +381,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) ATTN_SEG_TRACE(seg_no, 0, static_cast<long long>(global_timer_ns()));
                 if (lane == 0) ATTN_SEG_TRACE(seg_no, 6, s.kind * 1000000LL + (s.k1 - s.k0));
                 if (si.nmax == 0) continue;
-                if (!wait_all(&bar_q, segq & 1, ERRBIT_WAIT_Q)) {
+                if (!wait_all(&bar_k0_full, segq & 1, ERRBIT_WAIT_KV) || !wait_all(&bar_q, segq & 1, ERRBIT_WAIT_Q)) {
                     ok = false;
                     break;
                 }
-                if (lane == 0) ATTN_SEG_TRACE(seg_no, 1, static_cast<long long>(global_timer_ns()));
                 ++segq;
+                if (lane == 0) ATTN_SEG_TRACE(seg_no, 1, static_cast<long long>(global_timer_ns()));
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
@@ -364,6 +395,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             issue_S(t, dK0);
                             umma_commit(&bar_s_full[t]);
                         }
+                    umma_commit(&bar_k0_empty);
                 }
                 __syncwarp();
                 for (int jj = 0; jj < si.nmax; ++jj) {
@@ -412,7 +444,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ++g;
                 }
                 if (!ok) break;
-                // Q and the first K of this segment may be overwritten once these MMAs completed
+                // Q of this segment may be overwritten once these MMAs completed
                 if (elect_one()) umma_commit(&bar_q_empty);
                 __syncwarp();
                 if (lane == 0) ATTN_SEG_TRACE(seg_no, 2, static_cast<long long>(global_timer_ns()));
