@@ -40,25 +40,24 @@ bool get_encoder() {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: fp16 copy of V | per-chunk |V| maxima | per-head exponents | schedule batch offsets |
-// partial-result flags | partial results of split work units (each piece 256 B aligned).
+// Workspace: fp16 copy of V | per-tile V exponents | schedule batch offsets | partial-result flags |
+// partial results of split work units (each piece 256-byte aligned).
 struct WorkspaceLayout {
-    size_t v16 = 0, partial = 0, vexp = 0, boff = 0, flags = 0, part = 0, total = 0;
-    int chunks = 0;
+    size_t v16 = 0, vexp = 0, boff = 0, flags = 0, part = 0, total = 0;
+    int n_ktiles = 0;
 };
 
 bool workspace_layout(int B, int H_kv, int N, int d, WorkspaceLayout* w) {
     const long long elems_per_head = static_cast<long long>(N) * d;
     const long long heads = static_cast<long long>(B) * H_kv;
-    w->chunks = static_cast<int>((elems_per_head + attn_impl::VPREP_CHUNK - 1) / attn_impl::VPREP_CHUNK);
+    w->n_ktiles = (N + 127) / 128;
     w->v16 = 0;
-    w->partial = round_up(static_cast<size_t>(heads * elems_per_head) * 2, 256);
-    w->vexp = w->partial + round_up(static_cast<size_t>(heads) * w->chunks * sizeof(float), 256);
-    w->boff = w->vexp + round_up(static_cast<size_t>(heads) * sizeof(int32_t), 256);
+    w->vexp = round_up(static_cast<size_t>(heads * elems_per_head) * 2, 256);
+    w->boff = w->vexp + round_up(static_cast<size_t>(heads) * w->n_ktiles * sizeof(int32_t), 256);
     w->flags = w->boff + round_up(static_cast<size_t>(B + 1) * sizeof(long long), 256);
     w->part = w->flags + round_up(8 * attn_impl::SCHED_MAX_CTAS * sizeof(unsigned int), 256);
-    w->total = w->part + round_up(static_cast<size_t>(attn_impl::SCHED_MAX_CTAS) * 2 * (d + 2) * 128 * sizeof(float), 256);
-    return w->chunks <= 65535 && heads <= 65535;
+    w->total = w->part + round_up(static_cast<size_t>(attn_impl::SCHED_MAX_CTAS) * 2 * (d + 3) * 128 * sizeof(float), 256);
+    return heads < 65535;  // the pre-pass grid has heads + 1 rows of blocks
 }
 
 // SM count of the current device (cached per device).
@@ -163,10 +162,10 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     attn_impl::VPrepParams vp{};
     vp.V = V;
     vp.V16 = ws + w.v16;
-    vp.partial_max = reinterpret_cast<float*>(ws + w.partial);
     vp.v_exp = reinterpret_cast<int32_t*>(ws + w.vexp);
-    vp.elems_per_head = static_cast<long long>(N) * d;
-    vp.chunks = w.chunks;
+    vp.N = N;
+    vp.d = d;
+    vp.n_ktiles = w.n_ktiles;
     vp.heads = B * H_kv;
 
     CUtensorMap tmQ, tmK, tmV;
@@ -185,6 +184,7 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     p.LSE = LSE;
     p.kv_len = kv_len;
     p.v_exp = vp.v_exp;
+    p.n_ktiles = w.n_ktiles;
     p.boff = reinterpret_cast<const long long*>(ws + w.boff);
     p.part = reinterpret_cast<float*>(ws + w.part);
     p.flags = reinterpret_cast<unsigned int*>(ws + w.flags);
@@ -231,7 +231,7 @@ const char* attn_status_string(attn_status s) {
     return "ATTN_UNKNOWN_STATUS";
 }
 
-int attn_launches_per_call(attn_dtype in_dtype) { return in_dtype == ATTN_BF16 ? 3 : 1; }
+int attn_launches_per_call(attn_dtype in_dtype) { return in_dtype == ATTN_BF16 ? 2 : 1; }
 
 void attn_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs); }
 

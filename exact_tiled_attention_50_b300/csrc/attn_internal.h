@@ -187,7 +187,8 @@ struct TcParams {
     void* O;                  // [B,H,N,d] fp32 or bf16
     float* LSE;               // [B,H,N] or nullptr
     const int32_t* kv_len;    // [B] or nullptr
-    const int32_t* v_exp;     // [B*H_kv] power-of-two exponent of the fp16 copy of V
+    const int32_t* v_exp;     // [B*H_kv][n_ktiles] exponent e of each 128-key tile of the fp16 V copy
+    int n_ktiles;             // ceil(N / 128)
     const long long* boff;    // [B+1] line offset of each batch's first unit (plan pass)
     float* part;              // partial results [G][2][D + 2][128] (O columns, then m, then l; row fastest)
     unsigned int* flags;      // [G][2][4] partial-result ready flags (per CTA, tile, warp), zeroed by the plan pass
@@ -217,18 +218,14 @@ struct F32Params {
     float scale;
 };
 
-// V (bf16 [rows, d] per head) -> fp16 copy scaled by 2^-e per head (e chosen so |V| * 2^-e < 2^15).
+// V (bf16 [heads, N, d]) -> fp16 copy, one 128-row key tile at a time: tile j of head z is stored as
+// V * 2^-e[z][j], with e the smallest non-negative exponent that keeps |V| * 2^-e below 2^15.
 struct VPrepParams {
-    const void* V;            // bf16 [B*H_kv, N, d]
-    void* V16;                // fp16 [B*H_kv, N, d]
-    float* partial_max;       // [B*H_kv, chunks]
-    int32_t* v_exp;           // [B*H_kv]
-    long long elems_per_head; // N * d
-    int chunks;               // per head
-    int heads;                // B * H_kv
+    const void* V;            // bf16 [heads, N, d]
+    void* V16;                // fp16 [heads, N, d]
+    int32_t* v_exp;           // [heads, n_ktiles]
+    int N, d, n_ktiles, heads;
 };
-
-constexpr int VPREP_CHUNK = 16384;  // elements of V per CTA in the fp16 conversion
 
 cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStream_t stream);
 // tmO: fp32 output map (box 32 columns x 32 rows, 128-byte swizzle); unused for bf16 output.

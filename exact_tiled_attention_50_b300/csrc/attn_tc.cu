@@ -500,11 +500,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
             const int row = q0t + r;                   // query index
             const int row_lim = p.plan.causal ? min(kv_valid, row + 1) : kv_valid;  // keys < row_lim are valid
+            // per-tile exponents of the fp16 V copy; this piece's O holds sum P V * 2^-E with E the
+            // largest exponent of the tiles seen so far (the same for every row of the tile)
+            const int32_t* vexp_row = p.v_exp + static_cast<size_t>(s.b * p.H_kv + s.h / p.group) * p.n_ktiles;
+            int E = 0;
             float m_run = -INFINITY;                   // reference maximum (log2 domain, already scaled)
             float l_run = 0.f;                         // running sum of exp2(s*sl - m_run)
 
             for (int jj = 0; jj < nkvt; ++jj) {
                 const int j = k0 + jj;
+                const int e_j = __ldg(vexp_row + j);
                 // tcgen05.ld/st below are warp-collective: the warp proceeds only if every lane's wait
                 // succeeded
                 if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s, 0);
@@ -556,11 +561,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 bool rescale = false;
                 if (jj == 0) {
                     m_run = m_tile;
-                } else if (m_tile > m_run + RESCALE_THRESHOLD) {
-                    alpha = ex2_approx(m_run - m_tile);
-                    l_run *= alpha;
-                    m_run = m_tile;
-                    rescale = true;
+                    E = e_j;
+                } else {
+                    if (m_tile > m_run + RESCALE_THRESHOLD) {
+                        alpha = ex2_approx(m_run - m_tile);
+                        l_run *= alpha;
+                        m_run = m_tile;
+                        rescale = true;
+                    }
+                    if (e_j > E) {  // a tile of larger |V|: the accumulator moves to its exponent (exact)
+                        alpha = ldexpf(alpha, E - e_j);
+                        E = e_j;
+                        rescale = true;
+                    }
                 }
                 // Lazy rescale of O_t before any of this tile's P V lands in it (the previous P V into
                 // O_t has completed: its completion preceded the S_t commit this warpgroup waited on).
@@ -587,10 +600,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
                 // P = exp2(s * scale*log2e - m), written to TMEM as fp16 pairs over the first 64 columns
                 // of S_t, one half (64 keys) at a time; each half is announced as soon as it is stored.
-                // The scale-and-subtract and the row sum use two-wide fp32 instructions.
+                // The scale-and-subtract and the row sum use two-wide fp32 instructions. A tile whose
+                // V exponent is below E enters as P * 2^(e_j - E) (folded into the exponent); the row
+                // sum takes P itself.
                 {
+                    const int shift = e_j - E;  // <= 0, almost always 0
                     const f32x2 sl2 = make_f32x2(sl, sl);
-                    const f32x2 nm2 = make_f32x2(-m_sub, -m_sub);
+                    const f32x2 nm2 = make_f32x2(static_cast<float>(shift) - m_sub, static_cast<float>(shift) - m_sub);
                     f32x2 acc0 = make_f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
@@ -617,7 +633,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     float s0, s1, s2, s3;
                     split_f32x2(acc0, s0, s1);
                     split_f32x2(acc1, s2, s3);
-                    l_run += (s0 + s1) + (s2 + s3);
+                    const float psum = (s0 + s1) + (s2 + s3);
+                    l_run += shift == 0 ? psum : ldexpf(psum, -shift);
                 }
                 if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 6);
             }
@@ -642,7 +659,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
             if (s.kind == SEG_WRITER) {
                 // partial result for the owner of the unit: unnormalised O (row fastest), m, l
-                float* base = p.part + (static_cast<size_t>(blockIdx.x) * 2 + t) * (D + 2) * BLOCK_M;
+                float* base = p.part + (static_cast<size_t>(blockIdx.x) * 2 + t) * (D + 3) * BLOCK_M;
                 if (have) {
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
@@ -655,6 +672,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 base[D * BLOCK_M + r] = live ? m_run : -INFINITY;
                 base[(D + 1) * BLOCK_M + r] = live ? l_run : 0.f;
+                base[(D + 2) * BLOCK_M + r] = static_cast<float>(E);
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) {
@@ -672,6 +690,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int W = walk_sh[warp].W;
             int c_end = blockIdx.x + 1;
             float M = live ? m_run : -INFINITY;
+            int Emax = live ? E : -1000000;
             if (s.kind == SEG_OWNER) {
                 while (c_end < G && sched_chunk_start(p.plan, W, c_end) < s.unit_end) ++c_end;
                 for (int c2 = blockIdx.x + 1; c2 < c_end && ok; ++c2) {
@@ -681,26 +700,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 2) * BLOCK_M;
-                    if (__ldcg(b2 + (D + 1) * BLOCK_M + r) > 0.f) M = fmaxf(M, __ldcg(b2 + D * BLOCK_M + r));
+                    const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 3) * BLOCK_M;
+                    if (__ldcg(b2 + (D + 1) * BLOCK_M + r) > 0.f) {
+                        M = fmaxf(M, __ldcg(b2 + D * BLOCK_M + r));
+                        Emax = max(Emax, static_cast<int>(__ldcg(b2 + (D + 2) * BLOCK_M + r)));
+                    }
                 }
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
             }
-            const float w_own = live ? ex2_approx(m_run - M) : 0.f;
-            float L = w_own * l_run;
+            // softmax merge of the pieces: weights 2^(m_i - M) on l, 2^(m_i - M + E_i - Emax) on O
+            const float w_own_l = live ? ex2_approx(m_run - M) : 0.f;
+            const float w_own = live ? ldexpf(w_own_l, E - Emax) : 0.f;
+            float L = w_own_l * l_run;
             for (int c2 = blockIdx.x + 1; c2 < c_end; ++c2) {
-                const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 2) * BLOCK_M;
+                const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 3) * BLOCK_M;
                 if (sched_chunk_start(p.plan, W, c2 + 1) <= sched_chunk_start(p.plan, W, c2)) continue;
                 const float l2 = __ldcg(b2 + (D + 1) * BLOCK_M + r);
                 if (l2 > 0.f) L += ex2_approx(__ldcg(b2 + D * BLOCK_M + r) - M) * l2;
             }
             const int bh = s.b * p.plan.H + s.h;
-            const int zkv = s.b * p.H_kv + s.h / p.group;
-            const float vscale = ldexpf(1.0f, __ldg(p.v_exp + zkv));
-            const float inv = L > 0.f ? vscale / L : 0.f;
+            const float inv = L > 0.f ? ldexpf(1.0f, Emax) / L : 0.f;
             const bool store = row < p.plan.N;
             const size_t obase = (static_cast<size_t>(bh) * p.plan.N + (store ? row : 0)) * D;
             const uint32_t stage_base = smem_u32(smem + t * C::TILE_BYTES + wq * C::EPI_BUFS * 4096);
@@ -719,9 +741,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(have ? __uint_as_float(o[i]) * w_own : 0.f);
                 for (int c2 = blockIdx.x + 1; c2 < c_end; ++c2) {
                     if (sched_chunk_start(p.plan, W, c2 + 1) <= sched_chunk_start(p.plan, W, c2)) continue;
-                    const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 2) * BLOCK_M;
+                    const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 3) * BLOCK_M;
                     if (!(__ldcg(b2 + (D + 1) * BLOCK_M + r) > 0.f)) continue;
-                    const float w2 = ex2_approx(__ldcg(b2 + D * BLOCK_M + r) - M);
+                    const float w2 = ldexpf(ex2_approx(__ldcg(b2 + D * BLOCK_M + r) - M),
+                                            static_cast<int>(__ldcg(b2 + (D + 2) * BLOCK_M + r)) - Emax);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         o[i] = __float_as_uint(fmaf(w2, __ldcg(b2 + (c * 32 + i) * BLOCK_M + r), __uint_as_float(o[i])));
@@ -798,8 +821,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// V -> fp16 with a per-head power-of-two scale: pass 1 takes |V| maxima per chunk, pass 2 picks
-// the head's exponent e (so that |V| * 2^-e < 2^15) and writes V * 2^-e rounded to fp16.
+// V -> fp16, one 128-row key tile per CTA (a single pass: the tile stays in registers between its
+// |V| maximum and the conversion). The tile's exponent e keeps |V| * 2^-e < 2^15; values too small
+// for fp16 lose only absolute precision far below the result's rounding (below 2^-25 |V|max).
 // ---------------------------------------------------------------------------------------------
 // The schedule's batch offsets: boff[b] = sum over b' < b of H * (one head's cost in batch b'),
 // computed by one block; it also clears the partial-result flags of the attention kernel.
@@ -834,81 +858,63 @@ __device__ void plan_block(const PlanParams& pl) {
     for (int i = tid; i < 8 * SCHED_MAX_CTAS; i += 256) pl.flags[i] = 0u;
 }
 
-__global__ void __launch_bounds__(256) vprep_absmax_kernel(const VPrepParams p, const PlanParams pl) {
-    const int chunk = blockIdx.x, head = blockIdx.y;
+constexpr int VPREP_THREADS = 256;
+constexpr int VPREP_VECS = 128 * 128 / 8 / VPREP_THREADS;  // 16-byte vectors per thread (d = 128)
+
+__global__ void __launch_bounds__(VPREP_THREADS) vprep_kernel(const VPrepParams p, const PlanParams pl) {
+    const int tile = blockIdx.x, head = blockIdx.y;
     if (head == p.heads) {  // the extra row of blocks: block 0 plans, the others have nothing to do
-        if (chunk == 0) plan_block(pl);
+        if (tile == 0) plan_block(pl);
         return;
     }
-    const long long base = static_cast<long long>(head) * p.elems_per_head + static_cast<long long>(chunk) * VPREP_CHUNK;
-    const long long end = min(base + VPREP_CHUNK, static_cast<long long>(head + 1) * p.elems_per_head);
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.V) + base);
-    const int nvec = static_cast<int>((end - base) / 8);  // N*d is a multiple of 64
-    float m = 0.f;
-    for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
-        uint4 u = __ldg(src + i);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            // bf16 -> fp32 is a 16-bit shift; |x| clears the sign bit
-            m = fmaxf(m, __uint_as_float((w[e] << 16) & 0x7fffffffu));
-            m = fmaxf(m, __uint_as_float(w[e] & 0x7fff0000u));
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    __shared__ float red[8];
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float r = red[0];
-        for (int i = 1; i < 8; ++i) r = fmaxf(r, red[i]);
-        p.partial_max[head * p.chunks + chunk] = r;
-    }
-}
-
-__global__ void __launch_bounds__(256) vprep_convert_kernel(const VPrepParams p) {
-    const int chunk = blockIdx.x, head = blockIdx.y;
-    __shared__ int e_sh;
-    if (threadIdx.x < 32) {
-        float m = 0.f;
-        for (int i = threadIdx.x; i < p.chunks; i += 32) m = fmaxf(m, p.partial_max[head * p.chunks + i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (threadIdx.x == 0) {
-            int E = 0;
-            // |V| < 2^E; NaN/Inf inputs keep e = 0 and propagate through the result
-            if (isfinite(m) && m > 0.f) (void)frexpf(m, &E);
-            const int e = E > 15 ? E - 15 : 0;
-            e_sh = e;
-            if (chunk == 0) p.v_exp[head] = e;
-        }
-    }
-    __syncthreads();
-    const float s = ldexpf(1.0f, -e_sh);
-    const long long base = static_cast<long long>(head) * p.elems_per_head + static_cast<long long>(chunk) * VPREP_CHUNK;
-    const long long end = min(base + VPREP_CHUNK, static_cast<long long>(head + 1) * p.elems_per_head);
+    const int rows = min(128, p.N - tile * 128);
+    const int nvec = rows * p.d / 8;  // d is a multiple of 64
+    const size_t base = (static_cast<size_t>(head) * p.N + static_cast<size_t>(tile) * 128) * p.d;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.V) + base);
     uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(p.V16) + base);
-    const int nvec = static_cast<int>((end - base) / 8);
-    for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
-        uint4 u = __ldg(src + i);
-        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint4 u[VPREP_VECS];
+    uint32_t mbits = 0;  // largest |V| as bf16 bits (the order of non-negative floats is that of their bits)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(w[e] << 16) * s;
-            const float hi = __uint_as_float(w[e] & 0xffff0000u) * s;
-            w[e] = pack_f16x2(lo, hi);
+    for (int k = 0; k < VPREP_VECS; ++k) {
+        const int i = threadIdx.x + k * VPREP_THREADS;
+        u[k] = i < nvec ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mbits = max(mbits, max(w[e] & 0x7fffu, (w[e] >> 16) & 0x7fffu));
+    }
+    mbits = __reduce_max_sync(0xffffffffu, mbits);
+    __shared__ uint32_t red[VPREP_THREADS / 32];
+    __shared__ int e_sh;
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mbits;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t m = 0;
+        for (int i = 0; i < VPREP_THREADS / 32; ++i) m = max(m, red[i]);
+        const int e8 = static_cast<int>((m >> 7) & 0xffu);  // biased exponent: |V| < 2^(e8 - 126)
+        const int e = (e8 == 0xff || e8 <= 141) ? 0 : e8 - 141;  // NaN/Inf propagate unscaled
+        e_sh = e;
+        p.v_exp[static_cast<size_t>(head) * p.n_ktiles + tile] = e;
+    }
+    __syncthreads();
+    const int e = e_sh;
+    const float sc = ldexpf(1.0f, -e);
+#pragma unroll
+    for (int k = 0; k < VPREP_VECS; ++k) {
+        const int i = threadIdx.x + k * VPREP_THREADS;
+        if (i >= nvec) continue;
+        uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float lo = __uint_as_float(w[q] << 16) * sc;
+            const float hi = __uint_as_float(w[q] & 0xffff0000u) * sc;
+            w[q] = pack_f16x2(lo, hi);
         }
         dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
 cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStream_t stream) {
-    vprep_absmax_kernel<<<dim3(p.chunks, p.heads + 1), 256, 0, stream>>>(p, plan);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    vprep_convert_kernel<<<dim3(p.chunks, p.heads), 256, 0, stream>>>(p);
+    vprep_kernel<<<dim3(p.n_ktiles, p.heads + 1), VPREP_THREADS, 0, stream>>>(p, plan);
     return cudaGetLastError();
 }
 

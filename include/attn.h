@@ -27,8 +27,9 @@
  *
  * Precision. fp32 inputs are computed in exact fp32 arithmetic (CUDA cores). bf16 inputs use the
  * tensor cores: Q K^T is exact bf16 products with fp32 accumulation; the softmax state (m, l) is
- * fp32 per row; the probabilities enter P V as fp16 and V is converted to fp16 with a per-head
- * power-of-two scale (exact for bf16 values in fp16 range), accumulating O in fp32.
+ * fp32 per row; the probabilities enter P V as fp16 and V is converted to fp16 with a power-of-two
+ * scale per 128-key tile (exact for bf16 values in fp16's normal range; the accumulator follows the
+ * largest tile exponent seen so far, like the running maximum), accumulating O in fp32.
  *
  * Ownership and asynchrony. The caller owns every buffer. The library never allocates device
  * memory in attn_fwd: bf16 inputs need a caller-provided workspace of attn_workspace_bytes() bytes
@@ -68,7 +69,8 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
 
 /*
  * Bytes of device workspace attn_fwd needs for these sizes (0 for fp32 inputs). For bf16 inputs it
- * holds the fp16 copy of V ([B, H_kv, N, d]) plus per-head range data. Returns 0 for invalid sizes.
+ * holds the fp16 copy of V ([B, H_kv, N, d]) with one power-of-two exponent per 128-key tile, the
+ * work schedule and the partial results of work units split between CTAs. Returns 0 for invalid sizes.
  */
 size_t attn_workspace_bytes(int B, int H, int H_kv, int N, int d, attn_dtype in_dtype);
 
@@ -105,8 +107,8 @@ uint32_t attn_debug_last_error_bits(void);
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status s);
 
-/* Number of kernel launches attn_fwd enqueues for these arguments (1 for fp32, 3 for bf16: the V
- * pre-pass with the schedule plan, the V conversion and the persistent attention kernel). */
+/* Number of kernel launches attn_fwd enqueues for these arguments (1 for fp32, 2 for bf16: the V
+ * conversion with the schedule plan, and the persistent attention kernel). */
 int attn_launches_per_call(attn_dtype in_dtype);
 
 /*

@@ -112,6 +112,28 @@ def test_large_v_values_use_the_per_head_scale():
     assert np.abs(rel).max() <= 2e-3 and np.abs(rel).mean() <= 2e-4
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_v_magnitude_varies_across_key_tiles(causal):
+    """Key tiles of very different |V|: the fp16 copy of V takes one power-of-two exponent per 128-key
+    tile, the accumulator follows the largest exponent seen (exactly, like the running maximum), and
+    work units split between CTAs merge pieces with different exponents. The error of each output is
+    bounded relative to the magnitude it is made of, sum_j P_ij |V_j| (fp16 P rounding is relative)."""
+    import oracle
+    x = inputs.custom(2, 4, 2, 1000, 128, causal=causal, seed=31)
+    v = x.v.float()
+    v[:, :, 128:256] *= 2.0 ** 10
+    v[:, :, 640:768] *= 2.0 ** 20
+    v[:, 1, 900:1000] *= 2.0 ** 17
+    x.v = v.to(torch.bfloat16)
+    O, L = parity.run_gpu(x)
+    O_ref, L_ref, P = oracle.attention(x.q, x.k, x.v, x.scale, causal=causal, return_p=True)
+    vabs = np.repeat(np.abs(x.v.float().numpy()).astype(np.float64), 2, axis=1)  # kv head of each query head
+    mag = np.einsum("bhij,bhjd->bhid", P, vabs)
+    err = np.abs(O.double().cpu().numpy() - O_ref)
+    assert np.all(err <= 2e-3 * mag + 1e-30), float(np.max(err / (mag + 1e-30)))
+    assert float(np.abs(L.cpu().numpy() - L_ref).max()) <= parity.LSE_TOL
+
+
 # ---------------------------------------------------------------- guard bands, determinism
 def test_guard_bands_untouched():
     from exact_tiled_attention_50_b300 import attn
