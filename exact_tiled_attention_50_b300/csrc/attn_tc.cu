@@ -57,7 +57,7 @@ __device__ long long g_attn_trace[3][TRACE_J][TRACE_EV];
         if (blockIdx.x == 0 && (j) < TRACE_J) g_attn_trace[role][j][ev] = clock64(); \
     } while (0)
 // per CTA and segment: global-timer stamps (ns) of segment events, for the whole grid
-constexpr int TRACE_CTAS = 160, TRACE_SEGS = 16, TRACE_SEG_EV = 8;
+constexpr int TRACE_CTAS = 160, TRACE_SEGS = 16, TRACE_SEG_EV = 12;
 __device__ long long g_attn_seg_trace[TRACE_CTAS][TRACE_SEGS][TRACE_SEG_EV];
 #define ATTN_SEG_TRACE(seg, ev, val)                                                          \
     do {                                                                                      \
@@ -691,6 +691,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int c_end = blockIdx.x + 1;
             float M = live ? m_run : -INFINITY;
             int Emax = live ? E : -1000000;
+            // The first two other pieces (the usual case) keep their m, l, E in registers so that each
+            // output chunk needs one round trip to L2; further pieces are re-read (rare).
+            int np = 0;
+            const float* pb0 = nullptr;
+            const float* pb1 = nullptr;
+            float pm0 = -INFINITY, pl0 = 0.f, pm1 = -INFINITY, pl1 = 0.f;
+            int pe0 = 0, pe1 = 0;
             if (s.kind == SEG_OWNER) {
                 while (c_end < G && sched_chunk_start(p.plan, W, c_end) < s.unit_end) ++c_end;
                 for (int c2 = blockIdx.x + 1; c2 < c_end && ok; ++c2) {
@@ -701,9 +708,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 3) * BLOCK_M;
-                    if (__ldcg(b2 + (D + 1) * BLOCK_M + r) > 0.f) {
-                        M = fmaxf(M, __ldcg(b2 + D * BLOCK_M + r));
-                        Emax = max(Emax, static_cast<int>(__ldcg(b2 + (D + 2) * BLOCK_M + r)));
+                    const float m2 = __ldcg(b2 + D * BLOCK_M + r);
+                    const float l2 = __ldcg(b2 + (D + 1) * BLOCK_M + r);
+                    const int e2 = static_cast<int>(__ldcg(b2 + (D + 2) * BLOCK_M + r));
+                    if (np == 0) {
+                        pb0 = b2; pm0 = m2; pl0 = l2; pe0 = e2;
+                    } else if (np == 1) {
+                        pb1 = b2; pm1 = m2; pl1 = l2; pe1 = e2;
+                    }
+                    ++np;
+                    if (l2 > 0.f) {
+                        M = fmaxf(M, m2);
+                        Emax = max(Emax, e2);
                     }
                 }
                 if (!__all_sync(0xffffffffu, ok)) {
@@ -711,16 +727,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
             }
+            if (t == 0 && r == 0) ATTN_SEG_TRACE(seg_no, 8, static_cast<long long>(global_timer_ns()));
             // softmax merge of the pieces: weights 2^(m_i - M) on l, 2^(m_i - M + E_i - Emax) on O
             const float w_own_l = live ? ex2_approx(m_run - M) : 0.f;
             const float w_own = live ? ldexpf(w_own_l, E - Emax) : 0.f;
-            float L = w_own_l * l_run;
-            for (int c2 = blockIdx.x + 1; c2 < c_end; ++c2) {
-                const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 3) * BLOCK_M;
-                if (sched_chunk_start(p.plan, W, c2 + 1) <= sched_chunk_start(p.plan, W, c2)) continue;
-                const float l2 = __ldcg(b2 + (D + 1) * BLOCK_M + r);
-                if (l2 > 0.f) L += ex2_approx(__ldcg(b2 + D * BLOCK_M + r) - M) * l2;
+            const float w0l = pl0 > 0.f ? ex2_approx(pm0 - M) : 0.f;
+            const float w1l = pl1 > 0.f ? ex2_approx(pm1 - M) : 0.f;
+            const float w0 = pl0 > 0.f ? ldexpf(w0l, pe0 - Emax) : 0.f;
+            const float w1 = pl1 > 0.f ? ldexpf(w1l, pe1 - Emax) : 0.f;
+            float L = w_own_l * l_run + w0l * pl0 + w1l * pl1;
+            int c_extra = c_end;  // first CTA whose piece is beyond the two kept in registers
+            if (np > 2) {
+                int k = 0;
+                for (int c2 = blockIdx.x + 1; c2 < c_end; ++c2) {
+                    if (sched_chunk_start(p.plan, W, c2 + 1) <= sched_chunk_start(p.plan, W, c2)) continue;
+                    if (++k == 3) {
+                        c_extra = c2;
+                        break;
+                    }
+                }
+                for (int c2 = c_extra; c2 < c_end; ++c2) {
+                    const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 3) * BLOCK_M;
+                    if (sched_chunk_start(p.plan, W, c2 + 1) <= sched_chunk_start(p.plan, W, c2)) continue;
+                    const float l2 = __ldcg(b2 + (D + 1) * BLOCK_M + r);
+                    if (l2 > 0.f) L += ex2_approx(__ldcg(b2 + D * BLOCK_M + r) - M) * l2;
+                }
             }
+            if (t == 0 && r == 0) ATTN_SEG_TRACE(seg_no, 9, static_cast<long long>(global_timer_ns()));
             const int bh = s.b * p.plan.H + s.h;
             const float inv = L > 0.f ? ldexpf(1.0f, Emax) / L : 0.f;
             const bool store = row < p.plan.N;
@@ -739,7 +772,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // o holds the merged, still unnormalised row values (fp32 bits)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(have ? __uint_as_float(o[i]) * w_own : 0.f);
-                for (int c2 = blockIdx.x + 1; c2 < c_end; ++c2) {
+                if (np > 0) {  // the first two other pieces: all loads of the chunk in flight together
+                    float v0[32], v1[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        v0[i] = w0 != 0.f ? __ldcg(pb0 + (c * 32 + i) * BLOCK_M + r) : 0.f;
+                        v1[i] = w1 != 0.f ? __ldcg(pb1 + (c * 32 + i) * BLOCK_M + r) : 0.f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __float_as_uint(fmaf(w1, v1[i], fmaf(w0, v0[i], __uint_as_float(o[i]))));
+                }
+                for (int c2 = c_extra; c2 < c_end; ++c2) {  // further pieces (rare)
                     if (sched_chunk_start(p.plan, W, c2 + 1) <= sched_chunk_start(p.plan, W, c2)) continue;
                     const float* b2 = p.part + (static_cast<size_t>(c2) * 2 + t) * (D + 3) * BLOCK_M;
                     if (!(__ldcg(b2 + (D + 1) * BLOCK_M + r) > 0.f)) continue;
@@ -802,6 +846,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float lse = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
                 p.LSE[static_cast<size_t>(bh) * p.plan.N + row] = lse;
             }
+            if (t == 0 && r == 0) ATTN_SEG_TRACE(seg_no, 10, static_cast<long long>(global_timer_ns()));
             if (lane == 0 && seg_loads_q) {
                 if (!OUT_BF16) bulk_wait_group_read<0>();  // the staging buffers may be overwritten
                 mbar_arrive(&bar_q_free[t]);
