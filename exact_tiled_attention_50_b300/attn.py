@@ -20,7 +20,7 @@ ATTN_F32, ATTN_BF16 = 0, 1
 EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_workspace_bytes", "attn_launches_per_call",
             "attn_debug_set_wait_limit_ns", "attn_debug_set_skip_kv_load", "attn_set_kernel_events",
             "attn_event_elapsed_ms", "attn_fwd_noalloc", "attn_debug_schedule",
-            "attn_debug_last_error_bits")
+            "attn_debug_last_error_bits", "attn_merge")
 
 
 class AttnError(RuntimeError):
@@ -39,6 +39,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd.restype = ci
     lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci, ci, vp]
     lib.attn_fwd_noalloc.restype = ci
+    lib.attn_merge.argtypes = [vp, vp, ci, ctypes.c_longlong, ci, vp, vp, vp]
+    lib.attn_merge.restype = ci
     lib.attn_check.argtypes = [vp]
     lib.attn_check.restype = ci
     lib.attn_status_string.argtypes = [ci]
@@ -151,6 +153,25 @@ def attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
                               _dtype_code(q.dtype), _dtype_code(out.dtype), stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_noalloc")
+
+
+def merge(o_parts: torch.Tensor, lse_parts: torch.Tensor):
+    """Merge attention results over disjoint key sets: o_parts [P, ..., d] fp32, lse_parts [P, ...] fp32
+    (CUDA, contiguous) -> (O [..., d], LSE [...])."""
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise TypeError("merge takes fp32 parts")
+    o_parts, lse_parts = o_parts.contiguous(), lse_parts.contiguous()
+    P, d = o_parts.shape[0], o_parts.shape[-1]
+    rows = lse_parts[0].numel()
+    if o_parts[0].numel() != rows * d or lse_parts.shape[0] != P:
+        raise ValueError("shape mismatch between o_parts and lse_parts")
+    out = torch.empty(o_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    stream = torch.cuda.current_stream(o_parts.device).cuda_stream
+    rc = lib.attn_merge(o_parts.data_ptr(), lse_parts.data_ptr(), P, rows, d, out.data_ptr(), lse.data_ptr(), stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_merge")
+    return out, lse
 
 
 def schedule(B: int, H: int, N: int, causal: bool, kv_len=None, sms: int = 148):

@@ -103,6 +103,55 @@ bool encode_out_map(CUtensorMap* m, void* base, int d, int rows, long long slabs
     return r == CUDA_SUCCESS;
 }
 
+// Tensor maps depend only on (base address, element type, d, rows, slabs, kind), so a small cache
+// keyed on those saves re-encoding them for buffers used again (the common case).
+struct MapKey {
+    const void* base;
+    int kind, d, rows;
+    long long slabs;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && kind == o.kind && d == o.d && rows == o.rows && slabs == o.slabs;
+    }
+};
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool used;
+};
+constexpr int kMapCache = 32;
+MapEntry g_map_cache[kMapCache];
+int g_map_next = 0;
+std::mutex g_map_mutex;
+
+enum { MAP_Q_BF16 = 0, MAP_K_BF16 = 1, MAP_V_F16 = 2, MAP_O_F32 = 3 };
+
+bool encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int d, int rows, long long slabs);
+bool encode_out_map(CUtensorMap* m, void* base, int d, int rows, long long slabs);
+
+bool get_map(CUtensorMap* m, int kind, const void* base, int d, int rows, long long slabs) {
+    const MapKey key{base, kind, d, rows, slabs};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mutex);
+        for (int i = 0; i < kMapCache; ++i)
+            if (g_map_cache[i].used && g_map_cache[i].key == key) {
+                *m = g_map_cache[i].map;
+                return true;
+            }
+    }
+    bool ok = false;
+    if (kind == MAP_O_F32) ok = encode_out_map(m, const_cast<void*>(base), d, rows, slabs);
+    else ok = encode_rows_map(m, base, kind == MAP_V_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              d, rows, slabs);
+    if (!ok) return false;
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    MapEntry& e = g_map_cache[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCache;
+    e.key = key;
+    e.map = *m;
+    e.used = true;
+    return true;
+}
+
 bool sizes_ok(int B, int H, int H_kv, int N, int d) {
     if (B <= 0 || H <= 0 || H_kv <= 0 || N <= 0) return false;
     if (H % H_kv != 0) return false;
@@ -169,13 +218,14 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     vp.heads = B * H_kv;
 
     CUtensorMap tmQ, tmK, tmV;
-    if (!encode_rows_map(&tmQ, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, N, static_cast<long long>(B) * H) ||
-        !encode_rows_map(&tmK, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, N, static_cast<long long>(B) * H_kv) ||
-        !encode_rows_map(&tmV, vp.V16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, d, N, static_cast<long long>(B) * H_kv))
+    if (!get_map(&tmQ, MAP_Q_BF16, Q, d, N, static_cast<long long>(B) * H) ||
+        !get_map(&tmK, MAP_K_BF16, K, d, N, static_cast<long long>(B) * H_kv) ||
+        !get_map(&tmV, MAP_V_F16, vp.V16, d, N, static_cast<long long>(B) * H_kv))
         return ATTN_ERR_UNSUPPORTED;
     CUtensorMap tmO;
     memset(&tmO, 0, sizeof(tmO));
-    if (out_dtype == ATTN_F32 && !encode_out_map(&tmO, O, d, N, static_cast<long long>(B) * H)) return ATTN_ERR_UNSUPPORTED;
+    if (out_dtype == ATTN_F32 && !get_map(&tmO, MAP_O_F32, O, d, N, static_cast<long long>(B) * H))
+        return ATTN_ERR_UNSUPPORTED;
 
     const int sms = device_sms();
     if (sms <= 0) return ATTN_ERR_CUDA;
@@ -209,6 +259,16 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
         return ATTN_ERR_CUDA;
     if (timed && cudaEventRecord(ev1, stream) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
+}
+
+attn_status attn_merge(const float* O_parts, const float* LSE_parts, int n_parts, long long rows, int d, float* O,
+                       float* LSE, cudaStream_t stream) {
+    if (!O_parts || !LSE_parts || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+    if (n_parts <= 0 || rows <= 0 || (d != 64 && d != 128)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(O_parts, 16) || !aligned(O, 16) || !aligned(LSE_parts, 4) || !aligned(LSE, 4)) return ATTN_ERR_INVALID_ARG;
+    return attn_impl::launch_attn_merge(O_parts, LSE_parts, n_parts, rows, d, O, LSE, stream) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
 }
 
 attn_status attn_check(cudaStream_t stream) {

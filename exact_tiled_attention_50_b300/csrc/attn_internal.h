@@ -237,6 +237,9 @@ SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms);
 long long plan_max_steps(int B, int H, int N, int causal);
 cudaError_t launch_attn_f32(int d, const F32Params& p, cudaStream_t stream);
 
+cudaError_t launch_attn_merge(const float* O_parts, const float* LSE_parts, int n_parts, long long rows, int d,
+                              float* O, float* LSE, cudaStream_t stream);
+
 // Device error word of the current device: read and clear (synchronous on `stream`).
 cudaError_t read_and_clear_error(uint32_t* out, cudaStream_t stream);
 

@@ -37,6 +37,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -967,14 +969,23 @@ template <int D, bool OUT_BF16>
 static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
     auto kern = attn_fwd_tc_kernel<D, OUT_BF16>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
+    cudaError_t e = cudaSuccess;
+    // once per device: shared-memory opt-in and the register check
+    static std::atomic<int> ready[64];
+    int dev = 0;
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    // The register split inside the kernel assumes exactly LAUNCH_REGS registers per thread at
-    // launch; with fewer, the softmax warpgroups' increase could never be granted.
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidKernelImage;
+    if (dev < 0 || dev >= 64 || ready[dev].load(std::memory_order_acquire) == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        // The register split inside the kernel assumes exactly LAUNCH_REGS registers per thread at
+        // launch; with fewer, the softmax warpgroups' increase could never be granted.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidKernelImage;
+        if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
+    }
     if (p.plan.G <= 0 || p.plan.G > SCHED_MAX_CTAS) return cudaErrorInvalidConfiguration;
     // Cooperative launch: every CTA is resident at once, so an owner CTA may wait (bounded) for the
     // partial results of the CTAs after it.

@@ -91,6 +91,24 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
                      attn_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Merge of attention results over disjoint key sets (split-KV or sequence-parallel attention: each
+ * part attends the same queries to its own keys). For every row,
+ *     LSE = log(sum_i exp(LSE_i)),   O = sum_i exp(LSE_i - LSE) O_i
+ * (the softmax merge rule of formula 2, "闪电注意力的数学原理", on "闪电注意力：革命性地提高
+ * Transformer效率", unite.ai; the intra/inter-block combination of "深入解析Blockwise Parallel
+ * Transformer在PyTorch中的实现与优化", qqiyuan.cn). A part with LSE = -inf contributes nothing; a row
+ * where every part has -inf gets O = 0, LSE = -inf.
+ *   O_parts   device fp32 [n_parts, rows, d]  (each part normalised, as attn_fwd writes O)
+ *   LSE_parts device fp32 [n_parts, rows]     (natural log, as attn_fwd writes LSE)
+ *   O, LSE    device fp32 [rows, d] and [rows]; must not overlap the inputs
+ *   d in {64, 128}; rows = B * H * N for attn_fwd outputs.
+ * Errors: NULL pointers, n_parts or rows <= 0, other d, misaligned pointers (16 bytes for O buffers)
+ * -> ATTN_ERR_INVALID_ARG without a launch; a failed launch -> ATTN_ERR_CUDA. Asynchronous on `stream`.
+ */
+attn_status attn_merge(const float* O_parts, const float* LSE_parts, int n_parts, long long rows, int d, float* O,
+                       float* LSE, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the calling device's error word. Returns ATTN_OK,
  * ATTN_ERR_TIMEOUT (a bounded wait inside a kernel ran out; the results of that call are invalid)
  * or ATTN_ERR_CUDA (the stream reported an error).

@@ -62,3 +62,26 @@ def attention_np(q, k, v, scale, causal=False, kv_len=None, return_p=False):
     if return_p:
         return O, LSE, P_all
     return O, LSE
+
+
+def merge_np(O_parts, LSE_parts):
+    """Combine attention results computed over disjoint key sets (fp64).
+
+    O_parts [P, ..., d] (each part normalised over its own keys), LSE_parts [P, ...] (natural log).
+    Softmax merge rule, formula 2 of "闪电注意力的数学原理" on "闪电注意力：革命性地提高Transformer效率"
+    (unite.ai), in its corrected form: with m = max_i LSE_i, the union's log-sum-exp is
+    m + ln(sum_i exp(LSE_i - m)) and its output is sum_i exp(LSE_i - LSE) O_i. Parts whose LSE is -inf
+    (no valid key) get weight 0; if every part is -inf the row is O = 0, LSE = -inf.
+    """
+    O_parts = np.asarray(O_parts, dtype=np.float64)
+    L = np.asarray(LSE_parts, dtype=np.float64)
+    m = L.max(axis=0)
+    has = np.isfinite(m)
+    m_safe = np.where(has, m, 0.0)
+    w = np.where(np.isfinite(L), np.exp(L - m_safe[None]), 0.0)
+    s = w.sum(axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(has, m_safe + np.log(np.where(has, s, 1.0)), -np.inf)
+        wn = np.where(has[None], w / np.where(has, s, 1.0)[None], 0.0)
+    O = (wn[..., None] * O_parts).sum(axis=0)
+    return O, lse

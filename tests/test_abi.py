@@ -73,5 +73,13 @@ def test_invalid_arguments_rejected_without_launch(lib, bad):
     assert _call(lib, **bad) == lib.ATTN_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("bad", [dict(O_parts=None), dict(n=0), dict(rows=0), dict(d=96), dict(O=4100)])
+def test_merge_invalid_arguments(lib, bad):
+    a = dict(O_parts=4096, L_parts=4096, n=2, rows=128, d=128, O=8192, L=8192)
+    a.update(bad)
+    assert lib.lib.attn_merge(a["O_parts"], a["L_parts"], a["n"], a["rows"], a["d"], a["O"], a["L"], None) == \
+        lib.ATTN_ERR_INVALID_ARG
+
+
 def test_unsupported_combination(lib):
     assert _call(lib, ind=0, outd=1) == lib.ATTN_ERR_UNSUPPORTED

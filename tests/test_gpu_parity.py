@@ -134,6 +134,43 @@ def test_v_magnitude_varies_across_key_tiles(causal):
     assert float(np.abs(L.cpu().numpy() - L_ref).max()) <= parity.LSE_TOL
 
 
+# ---------------------------------------------------------------- merge over disjoint key sets
+@pytest.mark.parametrize("d", [64, 128])
+def test_merge_kernel_against_oracle(d):
+    """attn_merge on fp64 oracle parts over keys [0, L) and [L, N) (rounded to fp32) equals the oracle
+    over all keys, within the fp32 bar; a part without keys contributes nothing."""
+    import oracle
+    from exact_tiled_attention_50_b300 import attn
+    x = inputs.custom(2, 4, 2, 300, d, dtype="f32", peaky=True, seed=17)
+    q, k, v = (t.numpy() for t in (x.q, x.k, x.v))
+    O_full, L_full = oracle.attention(q, k, v, x.scale)
+    for L in (0, 128, 171):
+        A = oracle.attention(q, k, v, x.scale, kv_len=[L, L])
+        Bp = oracle.attention(q, np.roll(k, -L, axis=2), np.roll(v, -L, axis=2), x.scale, kv_len=[300 - L] * 2)
+        Op = torch.tensor(np.stack([A[0], Bp[0]]), dtype=torch.float32, device="cuda")
+        Lp = torch.tensor(np.stack([A[1], Bp[1]]), dtype=torch.float32, device="cuda")
+        O, LSE = attn.merge(Op, Lp)
+        assert float(np.abs(O.double().cpu().numpy() - O_full).max()) <= 1e-5
+        assert float(np.abs(LSE.double().cpu().numpy() - L_full).max()) <= 1e-5
+
+
+def test_split_kv_attention_merged_on_gpu():
+    """Sequence-parallel use: two attn_fwd calls over disjoint key ranges (the second through rotated
+    K/V and kv_len), merged by attn_merge, equal attention over all keys (bf16 bar)."""
+    import oracle
+    from exact_tiled_attention_50_b300 import attn
+    x = inputs.custom(2, 8, 2, 1000, 128, peaky=True, seed=23)
+    L = 389
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    OA, LA = attn.attn_fwd(q, k, v, scale=x.scale, kv_len=torch.full((2,), L, dtype=torch.int32, device="cuda"))
+    OB, LB = attn.attn_fwd(q, torch.roll(k, -L, 2).contiguous(), torch.roll(v, -L, 2).contiguous(), scale=x.scale,
+                           kv_len=torch.full((2,), 1000 - L, dtype=torch.int32, device="cuda"))
+    O, LSE = attn.merge(torch.stack([OA, OB]), torch.stack([LA, LB]))
+    assert attn.check() == attn.ATTN_OK
+    O_ref, L_ref = oracle.attention(x.q, x.k, x.v, x.scale)
+    parity.compare(O, LSE, O_ref, L_ref, "bf16", what="split-KV merged")
+
+
 # ---------------------------------------------------------------- guard bands, determinism
 def test_guard_bands_untouched():
     from exact_tiled_attention_50_b300 import attn

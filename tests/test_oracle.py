@@ -135,3 +135,49 @@ def test_unmutated_copy_passes_every_pin():
 def test_planted_mistake_is_caught(name):
     m = _mutant(*MUTANTS[name])
     assert pins.failing_pins(m), f"no pin caught the planted mistake {name}"
+
+
+# ---------------------------------------------------------------- merge over disjoint key sets
+def _split_parts(q, k, v, scale, L):
+    """Attention over keys [0, L) and over keys [L, N) with the C oracle: the second set is made the
+    first N - L keys by rotating K and V (attention without a causal mask does not depend on the
+    order of the keys)."""
+    N = q.shape[2]
+    B = q.shape[0]
+    A = oracle.attention(q, k, v, scale, kv_len=[L] * B)
+    kr, vr = np.roll(k, -L, axis=2), np.roll(v, -L, axis=2)
+    Bp = oracle.attention(q, kr, vr, scale, kv_len=[N - L] * B)
+    return A, Bp
+
+
+@pytest.mark.parametrize("L", [0, 1, 37, 64, 99, 100])
+def test_merge_of_split_keys_equals_full_attention(L):
+    rng = np.random.default_rng(40 + L)
+    B, H, H_kv, N, d = 2, 4, 2, 100, 16
+    q = rng.standard_normal((B, H, N, d)).astype(np.float32)
+    k = (rng.standard_normal((B, H_kv, N, d)) * np.where(rng.random((B, H_kv, N, 1)) < 0.1, 8, 1)).astype(np.float32)
+    v = rng.standard_normal((B, H_kv, N, d)).astype(np.float32)
+    O_full, L_full = oracle.attention(q, k, v, 0.25)
+    (OA, LA), (OB, LB) = _split_parts(q, k, v, 0.25, L)
+    O, LSE = oracle.merge_np(np.stack([OA, OB]), np.stack([LA, LB]))
+    np.testing.assert_allclose(O, O_full, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSE, L_full, rtol=0, atol=1e-12)
+
+
+def test_merge_special_cases():
+    rng = np.random.default_rng(7)
+    O1 = rng.standard_normal((3, 5, 8))
+    L1 = rng.standard_normal((3, 5))
+    O, L = oracle.merge_np(O1[None], L1[None])  # one part: unchanged
+    np.testing.assert_allclose(O, O1, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(L, L1, rtol=0, atol=1e-15)
+    empty = np.full_like(L1, -np.inf)  # a part without keys contributes nothing
+    O, L = oracle.merge_np(np.stack([O1, np.zeros_like(O1)]), np.stack([L1, empty]))
+    np.testing.assert_allclose(O, O1, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(L, L1, rtol=0, atol=1e-15)
+    O, L = oracle.merge_np(np.stack([O1, O1]), np.stack([empty, empty]))  # no keys anywhere
+    assert np.all(O == 0) and np.all(L == -np.inf)
+    # two equal parts: same output, LSE + ln 2
+    O, L = oracle.merge_np(np.stack([O1, O1]), np.stack([L1, L1]))
+    np.testing.assert_allclose(O, O1, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(L, L1 + np.log(2.0), rtol=0, atol=1e-14)
