@@ -6,8 +6,8 @@ the CUDA path; the two meet only in the seeded inputs of ``exact_tiled_attention
 
 ``attn_oracle.c`` is the plain definition (full N x N score matrix per head, fp64) plus a row-sampled
 evaluator of the same definition and a tiled restatement of the online-softmax recurrence;
-``attn_oracle_np.py`` is an independent NumPy restatement for small cases, and the merge of results
-over disjoint key sets (split-KV).
+``attn_oracle_np.py`` is an independent NumPy restatement for small cases, the merge of results over
+disjoint key sets (split-KV), and the backward pass (dQ, dK, dV) of the same attention.
 """
 from __future__ import annotations
 
@@ -135,4 +135,4 @@ def attention_tiled(q, k, v, scale, causal=False, kv_len=None, Br=16, Bc=16):
     return O, LSE
 
 
-from .attn_oracle_np import attention_np, merge_np  # noqa: E402  (independent NumPy restatement)
+from .attn_oracle_np import attention_bwd_np, attention_np, merge_np  # noqa: E402  (NumPy restatement)

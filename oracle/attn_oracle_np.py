@@ -85,3 +85,39 @@ def merge_np(O_parts, LSE_parts):
         wn = np.where(has[None], w / np.where(has, s, 1.0)[None], 0.0)
     O = (wn[..., None] * O_parts).sum(axis=0)
     return O, lse
+
+
+def attention_bwd_np(q, k, v, dO, scale, causal=False, kv_len=None):
+    """Gradients of the attention output with respect to Q, K and V (fp64).
+
+    The pages give the forward only; the backward of the same exact attention is the chain rule
+    through it, in the recompute form the pages motivate (the score matrix is not stored; P is
+    rebuilt from the row log-sum-exp): with P = softmax(S), S = scale Q K^T (masked), O = P V,
+        dV = P^T dO,   dP = dO V^T,   D_i = sum_c dO_ic O_ic,   dS = P * (dP - D),
+        dQ = scale dS K,   dK = scale dS^T Q.
+    Grouped heads: dK and dV of a key/value head sum over the query heads that read it. Rows without
+    valid keys contribute nothing. Returns dQ [B,H,N,d], dK [B,H_kv,N,d], dV [B,H_kv,N,d].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    dO = np.asarray(dO, dtype=np.float64)
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    g = H // H_kv
+    _, _, P = attention_np(q, k, v, scale, causal=causal, kv_len=kv_len, return_p=True)
+    dQ = np.zeros_like(q)
+    dK = np.zeros_like(k)
+    dV = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            kh = h // g
+            Pm = P[b, h]
+            O = Pm @ v[b, kh]
+            dV[b, kh] += Pm.T @ dO[b, h]
+            dP = dO[b, h] @ v[b, kh].T
+            D = np.sum(dO[b, h] * O, axis=1)
+            dS = Pm * (dP - D[:, None])
+            dQ[b, h] = float(scale) * (dS @ k[b, kh])
+            dK[b, kh] += float(scale) * (dS.T @ q[b, h])
+    return dQ, dK, dV
