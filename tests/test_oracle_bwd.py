@@ -93,7 +93,7 @@ BWD_MUTANTS = {
     "no_D": ("dS = Pm * (dP - D[:, None])", "dS = Pm * dP"),
     "dK_untransposed": ("dK[b, kh] += float(scale) * (dS.T @ q[b, h])", "dK[b, kh] += float(scale) * (dS @ q[b, h])"),
     "dQ_no_scale": ("dQ[b, h] = float(scale) * (dS @ k[b, kh])", "dQ[b, h] = (dS @ k[b, kh])"),
-    "dV_from_dP": ("dV[b, kh] += Pm.T @ dO[b, h]", "dV[b, kh] += dP.T @ dO[b, h]"),
+    "dV_untransposed": ("dV[b, kh] += Pm.T @ dO[b, h]", "dV[b, kh] += Pm @ dO[b, h]"),
     "gqa_overwrite": ("dK[b, kh] += float(scale)", "dK[b, kh] = float(scale)"),
 }
 
