@@ -20,7 +20,7 @@ ATTN_F32, ATTN_BF16 = 0, 1
 EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_workspace_bytes", "attn_launches_per_call",
             "attn_debug_set_wait_limit_ns", "attn_debug_set_skip_kv_load", "attn_set_kernel_events",
             "attn_event_elapsed_ms", "attn_fwd_noalloc", "attn_debug_schedule",
-            "attn_debug_last_error_bits", "attn_merge")
+            "attn_debug_last_error_bits", "attn_merge", "attn_bwd", "attn_bwd_workspace_bytes")
 
 
 class AttnError(RuntimeError):
@@ -39,6 +39,10 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd.restype = ci
     lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci, ci, vp]
     lib.attn_fwd_noalloc.restype = ci
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, vp, sz, vp]
+    lib.attn_bwd.restype = ci
+    lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
+    lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_merge.argtypes = [vp, vp, ci, ctypes.c_longlong, ci, vp, vp, vp]
     lib.attn_merge.restype = ci
     lib.attn_check.argtypes = [vp]
@@ -153,6 +157,36 @@ def attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
                               _dtype_code(q.dtype), _dtype_code(out.dtype), stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_noalloc")
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, do: torch.Tensor,
+             lse: torch.Tensor, *, scale: Optional[float] = None, causal: bool = False,
+             kv_len: Optional[torch.Tensor] = None):
+    """Gradients (dQ, dK, dV, fp32) of attn_fwd's output for upstream gradient do; q, k, v, do bf16,
+    o and lse the fp32 outputs of attn_fwd on the same inputs."""
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if not (q.dtype == k.dtype == v.dtype == do.dtype == torch.bfloat16):
+        raise TypeError("attn_bwd takes bf16 q, k, v, do")
+    if o.dtype != torch.float32 or lse.dtype != torch.float32:
+        raise TypeError("attn_bwd takes the fp32 O and LSE of attn_fwd")
+    q, k, v, o, do, lse = (t.contiguous() for t in (q, k, v, o, do, lse))
+    if scale is None:
+        scale = d ** -0.5
+    if kv_len is not None:
+        kv_len = kv_len.to(device=q.device, dtype=torch.int32).contiguous()
+    dq = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+    dk = torch.empty((B, H_kv, N, d), dtype=torch.float32, device=q.device)
+    dv = torch.empty((B, H_kv, N, d), dtype=torch.float32, device=q.device)
+    nbytes = int(lib.attn_bwd_workspace_bytes(B, H, N, d))
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, H_kv, N, d, float(scale), int(bool(causal)),
+                      kv_len.data_ptr() if kv_len is not None else None, ws.data_ptr(), nbytes, stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def merge(o_parts: torch.Tensor, lse_parts: torch.Tensor):

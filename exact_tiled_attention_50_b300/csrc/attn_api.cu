@@ -271,9 +271,58 @@ attn_status attn_merge(const float* O_parts, const float* LSE_parts, int n_parts
                : ATTN_ERR_CUDA;
 }
 
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+    const size_t nqp = static_cast<size_t>((N + 127) / 128) * 128;
+    return 2 * round_up(static_cast<size_t>(B) * H * nqp * sizeof(float), 256);
+}
+
+attn_status attn_bwd(const void* Q, const void* K, const void* V, const float* O, const void* dO, const float* LSE,
+                     float* dQ, float* dK, float* dV, int B, int H, int H_kv, int N, int d, float scale, int causal,
+                     const int32_t* kv_len, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
+    if (!sizes_ok(B, H, H_kv, N, d)) return ATTN_ERR_INVALID_ARG;
+    if (!(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(dO, 16) || !aligned(O, 16) ||
+        !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) || !aligned(LSE, 4))
+        return ATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return ATTN_ERR_INVALID_ARG;
+    const size_t need = attn_bwd_workspace_bytes(B, H, N, d);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H_kv > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (!get_encoder()) return ATTN_ERR_CUDA;
+    const int n_qt = (N + 127) / 128;
+    const size_t half = need / 2;
+    float* lse2 = static_cast<float*>(workspace);
+    float* dvec = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + half);
+
+    CUtensorMap tmQ, tmK, tmV, tmDO, tmDQ;
+    if (!get_map(&tmQ, MAP_Q_BF16, Q, d, N, static_cast<long long>(B) * H) ||
+        !get_map(&tmK, MAP_K_BF16, K, d, N, static_cast<long long>(B) * H_kv) ||
+        !get_map(&tmV, MAP_K_BF16, V, d, N, static_cast<long long>(B) * H_kv) ||
+        !get_map(&tmDO, MAP_Q_BF16, dO, d, N, static_cast<long long>(B) * H) ||
+        !get_map(&tmDQ, MAP_O_F32, dQ, d, N, static_cast<long long>(B) * H))
+        return ATTN_ERR_UNSUPPORTED;
+
+    attn_impl::BwdPrepParams pp{};
+    pp.dO = dO; pp.O = O; pp.LSE = LSE; pp.lse2 = lse2; pp.dvec = dvec; pp.dQ = dQ;
+    pp.rows = B * H; pp.N = N; pp.d = d; pp.NQP = n_qt * 128;
+    attn_impl::BwdParams p{};
+    p.dQ = dQ; p.dK = dK; p.dV = dV; p.lse2 = lse2; p.dvec = dvec; p.kv_len = kv_len;
+    p.B = B; p.H = H; p.H_kv = H_kv; p.N = N; p.group = H / H_kv; p.causal = causal; p.n_qt = n_qt;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    return attn_impl::launch_attn_bwd(d, pp, tmQ, tmK, tmV, tmDO, tmDQ, p, stream) == cudaSuccess ? ATTN_OK
+                                                                                                : ATTN_ERR_CUDA;
+}
+
 attn_status attn_check(cudaStream_t stream) {
-    uint32_t bits = 0;
+    uint32_t bits = 0, bwd_bits = 0;
     if (attn_impl::read_and_clear_error(&bits, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (attn_impl::read_and_clear_bwd_error(&bwd_bits) != cudaSuccess) return ATTN_ERR_CUDA;
+    bits |= bwd_bits;
     g_last_error_bits.store(bits);
     return bits ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }

@@ -1,0 +1,423 @@
+// Tensor-core attention backward for bf16 inputs on sm_103a (B300): dQ, dK, dV.
+//
+// The pages state the forward pass; its gradient is the chain rule through the same exact attention,
+// in the recompute form of "闪电注意力：革命性地提高Transformer效率" (unite.ai, the key ideas: do not
+// store the attention matrix, recompute its parts in the backward pass) with the row log-sum-exp of
+// the forward: P = exp(scale Q K^T - LSE) (masked), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
+// dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+//
+// Blackwell mapping: one CTA per (key tile of 128 keys, batch, kv head); it keeps K_j and V_j in
+// shared memory and accumulates dK_j and dV_j in tensor memory over every query head of its group and
+// every query tile (causal: the tiles at or after the key tile). Per query tile:
+//   MMA warp      S^T = K_j Q_i^T, dP^T = V_j dO_i^T         (TMEM cols 0-127, 128-255)
+//   warps 0-3     one key row each: P^T, dS^T -> bf16 in shared memory (128-byte swizzled)
+//   MMA warp      dV += P^T dO_i, dK += dS^T Q_i, dQ_i = dS K_j   (dQ in cols 0-127)
+//   warps 4-7     one query row each: dQ_i scaled and atomically added into the fp32 dQ in device
+//                 memory (several key tiles add into the same rows)
+//   warp 9        TMA loads (K_j, V_j once; Q_i, dO_i and the row statistics per tile)
+// All waits are bounded as in the forward kernel; a wait that runs out records an error bit.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attn_impl {
+
+using namespace attn_sm103;
+
+__device__ unsigned int g_attn_bwd_error = 0;
+
+namespace {
+
+constexpr int BW_THREADS = 384;
+constexpr int BW_MMA_WARP = 8;
+constexpr int BW_TMA_WARP = 9;
+
+template <int D>
+struct BwCfg {
+    static constexpr int NB = D / 64;
+    static constexpr int TILE = NB * 16384;   // 128 rows x D 16-bit values
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = TILE;
+    static constexpr int OFF_Q = 2 * TILE;
+    static constexpr int OFF_DO = 3 * TILE;
+    static constexpr int OFF_PT = 4 * TILE;   // P^T  [128 keys][128 queries] bf16
+    static constexpr int OFF_DST = OFF_PT + 32768;  // dS^T [128 keys][128 queries] bf16
+    static constexpr int OFF_STAT = OFF_DST + 32768;  // lse2[128], dvec[128]
+    static constexpr int SMEM = 1024 + OFF_STAT + 1024;
+    static constexpr uint32_t IDESC_SD = idesc_f16(128, 128, 1, 1, 0, 0);  // S^T, dP^T: K-major A and B
+    static constexpr uint32_t IDESC_KV = idesc_f16(128, D, 1, 1, 0, 1);    // dV, dK: A K-major, B MN-major
+    static constexpr uint32_t IDESC_Q = idesc_f16(128, D, 1, 1, 1, 1);     // dQ: A (dS) and B (K) MN-major
+    static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 384, T_DQ = 0;
+};
+
+__device__ __forceinline__ void bw_fail(volatile int* abort_flag, uint32_t bits) {
+    *abort_flag = 1;
+    atomicOr(&g_attn_bwd_error, ERRBIT_TIMEOUT | bits);
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(BW_THREADS, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdParams p) {
+    using C = BwCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bar_kv, bar_qdo_full, bar_qdo_empty, bar_s_full, bar_ps_full, bar_ps_empty,
+        bar_dq_full, bar_dq_free, bar_done;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int jt = blockIdx.x;                 // key tile
+    const int zkv = blockIdx.y;                // b * H_kv + kv head
+    const int b = zkv / p.H_kv, hk = zkv - b * p.H_kv;
+    const int N = p.N;
+    int kv_valid = N;
+    if (p.kv_len) {
+        kv_valid = __ldg(p.kv_len + b);
+        kv_valid = kv_valid < 0 ? 0 : (kv_valid > N ? N : kv_valid);
+    }
+    const int k0 = jt * 128;
+    const bool any_keys = k0 < kv_valid;
+    const int i_first = p.causal ? jt : 0;     // query tiles with at least one valid pair
+    const int n_i = any_keys ? p.n_qt - i_first : 0;
+    const int n_steps = n_i * p.group;         // (query head of the group, query tile) pairs
+    const uint64_t limit_ns = p.wait_limit_ns;
+
+    if (warp == BW_MMA_WARP) {
+        tmem_alloc(&tmem_base_sh, 512);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(&bar_kv, 1);
+        mbar_init(&bar_qdo_full, 1);
+        mbar_init(&bar_qdo_empty, 1);
+        mbar_init(&bar_s_full, 1);
+        mbar_init(&bar_ps_full, 128);
+        mbar_init(&bar_ps_empty, 1);
+        mbar_init(&bar_dq_full, 1);
+        mbar_init(&bar_dq_free, 128);
+        mbar_init(&bar_done, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    // step s -> (query head, query tile)
+    auto step_head = [&](int s) { return hk * p.group + s / n_i; };
+    auto step_tile = [&](int s) { return i_first + s % n_i; };
+
+    if (warp == BW_TMA_WARP) {
+        // ====================================== TMA producer ======================================
+        if (elect_one() && n_steps > 0) {
+            mbar_arrive_expect_tx(&bar_kv, 2 * C::TILE);
+            for (int bx = 0; bx < C::NB; ++bx) {
+                tma_load_3d(smem + C::OFF_K + bx * 16384, &tmK, &bar_kv, bx * 64, k0, zkv);
+                tma_load_3d(smem + C::OFF_V + bx * 16384, &tmV, &bar_kv, bx * 64, k0, zkv);
+            }
+            int issued = 0;
+            for (int s = 0; s < n_steps; ++s) {
+                if (s > 0 && !mbar_wait(&bar_qdo_empty, (s - 1) & 1, limit_ns, &abort_flag)) {
+                    bw_fail(&abort_flag, ERRBIT_WAIT_EMPTY);
+                    break;
+                }
+                const int bh = b * p.H + step_head(s), it = step_tile(s);
+                mbar_arrive_expect_tx(&bar_qdo_full, 2 * C::TILE + 1024);
+                for (int bx = 0; bx < C::NB; ++bx) {
+                    tma_load_3d(smem + C::OFF_Q + bx * 16384, &tmQ, &bar_qdo_full, bx * 64, it * 128, bh);
+                    tma_load_3d(smem + C::OFF_DO + bx * 16384, &tmDO, &bar_qdo_full, bx * 64, it * 128, bh);
+                }
+                const size_t srow = static_cast<size_t>(bh) * p.n_qt * 128 + static_cast<size_t>(it) * 128;
+                bulk_load(smem + C::OFF_STAT, p.lse2 + srow, 512, &bar_qdo_full);
+                bulk_load(smem + C::OFF_STAT + 512, p.dvec + srow, 512, &bar_qdo_full);
+                issued = s + 1;
+            }
+            if (abort_flag) {  // wait (bounded) for the copies in flight before the CTA may exit
+                volatile int never = 0;
+                (void)mbar_wait(&bar_kv, 0, limit_ns, &never);
+                if (issued > 0) (void)mbar_wait(&bar_qdo_full, (issued - 1) & 1, limit_ns, &never);
+            }
+        }
+        __syncwarp();
+    } else if (warp == BW_MMA_WARP) {
+        // ======================================= MMA issuer =======================================
+        auto wait_all = [&](uint64_t* bar, uint32_t parity, uint32_t bit) {
+            const bool got = mbar_wait(bar, parity, limit_ns, &abort_flag);
+            if (__all_sync(0xffffffffu, got)) return true;
+            if (!got) bw_fail(&abort_flag, bit);
+            return false;
+        };
+        const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);      // K as K-major A
+        const uint64_t dV_k = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);      // V as K-major A
+        const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);      // Q as K-major B
+        const uint64_t dDO_k = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);    // dO as K-major B
+        const uint64_t dQ_mn = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16384, 1024);  // Q as MN-major B
+        const uint64_t dDO_mn = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16384, 1024);
+        const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + C::OFF_K), 16384, 1024);  // K as MN-major B
+        const uint64_t dPT_k = sdesc_sw128(smem_u32(smem + C::OFF_PT), 16, 1024);    // P^T as K-major A
+        const uint64_t dDST_k = sdesc_sw128(smem_u32(smem + C::OFF_DST), 16, 1024);  // dS^T as K-major A
+        const uint64_t dDS_mn = sdesc_sw128(smem_u32(smem + C::OFF_DST), 16384, 1024);  // dS as MN-major A
+        // K-major operand over a 128 (or D) deep contraction: k-step kk of 16 elements
+        auto kmaj = [](int kk) { return static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
+        auto mnmaj = [](int kk) { return static_cast<uint64_t>((kk * 2048) >> 4); };
+        bool ok = n_steps > 0 ? wait_all(&bar_kv, 0, ERRBIT_WAIT_KV) : true;
+        for (int s = 0; s < n_steps && ok; ++s) {
+            if (!wait_all(&bar_qdo_full, s & 1, ERRBIT_WAIT_Q)) { ok = false; break; }
+            if (s > 0 && !wait_all(&bar_dq_free, (s - 1) & 1, ERRBIT_WAIT_O)) { ok = false; break; }
+            tc_fence_after();
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_ss(tmem + C::T_S, dK_k + kmaj(kk), dQ_k + kmaj(kk), C::IDESC_SD, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_ss(tmem + C::T_DP, dV_k + kmaj(kk), dDO_k + kmaj(kk), C::IDESC_SD, kk > 0);
+                umma_commit(&bar_s_full);
+            }
+            __syncwarp();
+            if (!wait_all(&bar_ps_full, s & 1, ERRBIT_WAIT_P)) { ok = false; break; }
+            tc_fence_after();
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // contraction over the 128 queries
+                    umma_ss(tmem + C::T_DV, dPT_k + kmaj(kk), dDO_mn + mnmaj(kk), C::IDESC_KV, (s > 0 || kk > 0));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_ss(tmem + C::T_DK, dDST_k + kmaj(kk), dQ_mn + mnmaj(kk), C::IDESC_KV, (s > 0 || kk > 0));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // contraction over the 128 keys
+                    umma_ss(tmem + C::T_DQ, dDS_mn + mnmaj(kk), dK_mn + mnmaj(kk), C::IDESC_Q, kk > 0);
+                umma_commit(&bar_dq_full);
+                umma_commit(&bar_ps_empty);
+                umma_commit(&bar_qdo_empty);
+            }
+            __syncwarp();
+        }
+        if (elect_one()) umma_commit(&bar_done);  // every MMA issued above has completed
+        __syncwarp();
+        volatile int never = 0;
+        const bool drained = mbar_wait(&bar_done, 0, limit_ns, &never);
+        if (!__all_sync(0xffffffffu, drained) && lane == 0) bw_fail(&abort_flag, ERRBIT_WAIT_DRAIN);
+    } else if (warp < 4) {
+        // ============== warps 0-3: one key row each; P^T and dS^T into shared memory ==============
+        const int r = warp * 32 + lane;          // key row in the tile
+        const int key = k0 + r;
+        const uint32_t lane_off = tmem_lane_base(warp);
+        const float sl = p.scale_log2;
+        const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_STAT);
+        const float* dvec = lse2 + 128;
+        const uint32_t pt_row = smem_u32(smem + C::OFF_PT) + r * 128;
+        const uint32_t dst_row = smem_u32(smem + C::OFF_DST) + r * 128;
+        bool ok = true;
+        for (int s = 0; s < n_steps && ok; ++s) {
+            const int it = step_tile(s);
+            const int q0 = it * 128;
+            bool got = mbar_wait(&bar_s_full, s & 1, limit_ns, &abort_flag);
+            got = got && mbar_wait(&bar_qdo_full, s & 1, limit_ns, &abort_flag);
+            if (s > 0) got = got && mbar_wait(&bar_ps_empty, (s - 1) & 1, limit_ns, &abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_S);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {        // 32 queries at a time
+                uint32_t sv[32], dpv[32];
+                tmem_ld32(tmem + lane_off + C::T_S + c * 32, sv);
+                tmem_ld32(tmem + lane_off + C::T_DP + c * 32, dpv);
+                tmem_wait_ld(sv);
+                tmem_wait_ld(dpv);
+                uint32_t pp[16], dd[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int qi = c * 32 + i + u;
+                        const int q = q0 + qi;
+                        const bool valid = key < kv_valid && q < N && (!p.causal || key <= q);
+                        const float e = valid ? ex2_approx(__uint_as_float(sv[i + u]) * sl - lse2[qi]) : 0.f;
+                        pv[u] = e;
+                        dv[u] = e * (__uint_as_float(dpv[i + u]) - dvec[qi]);
+                    }
+                    __nv_bfloat162 ph = __floats2bfloat162_rn(pv[0], pv[1]);
+                    __nv_bfloat162 dh = __floats2bfloat162_rn(dv[0], dv[1]);
+                    pp[i / 2] = *reinterpret_cast<uint32_t*>(&ph);
+                    dd[i / 2] = *reinterpret_cast<uint32_t*>(&dh);
+                }
+                // 32 queries = four 16-byte chunks of this row; box c / 2, chunk (c % 2) * 4 + k
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int ch = (c & 1) * 4 + k;
+                    const uint32_t off = (c >> 1) * 16384 + ((ch ^ (r & 7)) << 4);
+                    st_shared_v4(pt_row + off, pp[4 * k], pp[4 * k + 1], pp[4 * k + 2], pp[4 * k + 3]);
+                    st_shared_v4(dst_row + off, dd[4 * k], dd[4 * k + 1], dd[4 * k + 2], dd[4 * k + 3]);
+                }
+            }
+            fence_proxy_async_smem();  // the MMAs read P^T and dS^T through the async proxy
+            tc_fence_before();
+            mbar_arrive(&bar_ps_full);
+        }
+        // ---- dK, dV of this key tile: fp32 rows straight to device memory ----
+        if (ok && n_steps > 0) {
+            const bool got = mbar_wait(&bar_done, 0, limit_ns, &abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_DRAIN);
+                ok = false;
+            }
+            tc_fence_after();
+        }
+        // ok and n_steps are warp-uniform; key < N is not (the last key tile of a ragged N), so every
+        // lane takes part in the warp-collective tensor-memory loads and only the stores are guarded.
+        if (ok) {
+            const bool row_ok = key < N;
+            const size_t orow = (static_cast<size_t>(zkv) * N + (row_ok ? key : 0)) * D;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                float* dst = (which ? p.dK : p.dV) + orow;
+                const float mul = which ? p.scale : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    if (n_steps > 0) {
+                        tmem_ld32(tmem + lane_off + (which ? C::T_DK : C::T_DV) + c * 32, v);
+                        tmem_wait_ld(v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                    }
+                    if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(dst + c * 32 + i) =
+                                make_float4(__uint_as_float(v[i]) * mul, __uint_as_float(v[i + 1]) * mul,
+                                            __uint_as_float(v[i + 2]) * mul, __uint_as_float(v[i + 3]) * mul);
+                    }
+                }
+            }
+        }
+    } else if (warp < 8) {
+        // ======= warps 4-7: one query row each; dQ_i scaled and atomically added into device memory =======
+        // (several key tiles add into the same dQ rows; fp32 reductions at L2, no bulk-group waits)
+        const int wq = warp & 3;
+        const uint32_t lane_off = tmem_lane_base(wq);
+        bool ok = true;
+        for (int s = 0; s < n_steps && ok; ++s) {
+            const bool got = mbar_wait(&bar_dq_full, s & 1, limit_ns, &abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_O);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int bh = b * p.H + step_head(s), it = step_tile(s);
+            const int q = it * 128 + wq * 32 + lane;
+            float* row = p.dQ + (static_cast<size_t>(bh) * N + (q < N ? q : 0)) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + C::T_DQ + c * 32, v);
+                tmem_wait_ld(v);
+                if (c == D / 32 - 1) {  // tensor memory read out: the next S^T may overwrite it
+                    tc_fence_before();
+                    mbar_arrive(&bar_dq_free);
+                }
+                if (q < N) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) atomicAdd(row + c * 32 + i, __uint_as_float(v[i]) * p.scale);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == BW_MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// D = rowsum(dO * O) and LSE in log2 units for every (padded) query row; dQ rows cleared.
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdPrepParams p) {
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // over bh * NQP
+    const int lane = threadIdx.x & 31;
+    if (row >= static_cast<long long>(p.rows) * p.NQP) return;
+    const int bh = static_cast<int>(row / p.NQP), i = static_cast<int>(row % p.NQP);
+    float dsum = 0.f;
+    float l2 = INFINITY;  // padding rows: P = exp2(x - inf) = 0
+    if (i < p.N) {
+        const size_t base = (static_cast<size_t>(bh) * p.N + i) * p.d;
+        const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(p.dO) + base;
+        for (int c = lane; c < p.d; c += 32) {
+            dsum = fmaf(__bfloat162float(dO[c]), p.O[base + c], dsum);
+            p.dQ[base + c] = 0.f;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+        const float lse = p.LSE[static_cast<size_t>(bh) * p.N + i];
+        l2 = lse * 1.4426950408889634f;
+    }
+    if (lane == 0) {
+        p.lse2[row] = l2;
+        p.dvec[row] = dsum;
+    }
+}
+
+template <int D>
+static cudaError_t launch_bwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                const CUtensorMap& tmDO, const CUtensorMap& tmDQ, const BwdParams& p,
+                                cudaStream_t stream) {
+    auto kern = attn_bwd_tc_kernel<D>;
+    static std::atomic<int> ready[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || ready[dev].load(std::memory_order_acquire) == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwCfg<D>::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
+    }
+    const dim3 grid(static_cast<unsigned>(p.n_qt), static_cast<unsigned>(p.B * p.H_kv));
+    attn_bwd_tc_kernel<D><<<grid, BW_THREADS, BwCfg<D>::SMEM, stream>>>(tmQ, tmK, tmV, tmDO, tmDQ, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd(int d, const BwdPrepParams& prep, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, const CUtensorMap& tmDO, const CUtensorMap& tmDQ,
+                            const BwdParams& p, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(prep.rows) * prep.NQP;
+    const long long blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL || p.B * p.H_kv > 65535) return cudaErrorInvalidConfiguration;
+    attn_bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(prep);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (d == 128) return launch_bwd_t<128>(tmQ, tmK, tmV, tmDO, tmDQ, p, stream);
+    if (d == 64) return launch_bwd_t<64>(tmQ, tmK, tmV, tmDO, tmDQ, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t read_and_clear_bwd_error(uint32_t* out) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_attn_bwd_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbol(g_attn_bwd_error, &zero, sizeof(zero));
+    *out = v;
+    return e;
+}
+
+}  // namespace attn_impl

@@ -240,6 +240,34 @@ cudaError_t launch_attn_f32(int d, const F32Params& p, cudaStream_t stream);
 cudaError_t launch_attn_merge(const float* O_parts, const float* LSE_parts, int n_parts, long long rows, int d,
                               float* O, float* LSE, cudaStream_t stream);
 
+// Backward pass (bf16 inputs): see attn_bwd.cu.
+struct BwdParams {
+    float* dQ;                // [B,H,N,d] fp32 (cleared by the prep kernel, reduce-added into)
+    float* dK;                // [B,H_kv,N,d] fp32
+    float* dV;                // [B,H_kv,N,d] fp32
+    const float* lse2;        // [B*H][n_qt*128] LSE * log2(e) (+inf on padding rows)
+    const float* dvec;        // [B*H][n_qt*128] rowsum(dO * O)
+    const int32_t* kv_len;    // [B] or nullptr
+    int B, H, H_kv, N, group, causal, n_qt;
+    float scale, scale_log2;
+    unsigned long long wait_limit_ns;
+};
+
+struct BwdPrepParams {
+    const void* dO;           // bf16 [B,H,N,d]
+    const float* O;           // fp32 [B,H,N,d]
+    const float* LSE;         // fp32 [B,H,N]
+    float* lse2;
+    float* dvec;
+    float* dQ;
+    int rows, N, d, NQP;      // rows = B*H, NQP = n_qt * 128
+};
+
+cudaError_t launch_attn_bwd(int d, const BwdPrepParams& prep, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, const CUtensorMap& tmDO, const CUtensorMap& tmDQ,
+                            const BwdParams& p, cudaStream_t stream);
+cudaError_t read_and_clear_bwd_error(uint32_t* out);
+
 // Device error word of the current device: read and clear (synchronous on `stream`).
 cudaError_t read_and_clear_error(uint32_t* out, cudaStream_t stream);
 

@@ -91,6 +91,27 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
                      attn_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Backward pass of attn_fwd (bf16 inputs): the gradients of the output O with respect to Q, K and V
+ * for an upstream gradient dO. The pages state the forward only; this is its chain rule in the
+ * recompute form of "闪电注意力：革命性地提高Transformer效率" (unite.ai: the attention matrix is not
+ * stored but rebuilt in the backward pass) from the forward's row log-sum-exp:
+ *     P = exp(scale Q K^T - LSE) (masked as in attn_fwd), dV = P^T dO, dP = dO V^T,
+ *     D = rowsum(dO * O), dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q;
+ * grouped heads sum dK and dV over the query heads of their group.
+ *   Q, dO      device bf16 [B, H, N, d];  K, V device bf16 [B, H_kv, N, d]
+ *   O, LSE     device fp32 [B, H, N, d] and [B, H, N]: attn_fwd's outputs for the same inputs
+ *   dQ         device fp32 [B, H, N, d]; dK, dV device fp32 [B, H_kv, N, d] (all overwritten)
+ *   scale, causal, kv_len as for attn_fwd; d in {64, 128}
+ *   workspace  device, attn_bwd_workspace_bytes() bytes, 256-byte aligned (row statistics)
+ * Precision: P and dS enter the tensor-core products as bf16 with fp32 accumulation. Errors: as
+ * attn_fwd (no launch on invalid arguments); bounded waits report ATTN_ERR_TIMEOUT via attn_check.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+attn_status attn_bwd(const void* Q, const void* K, const void* V, const float* O, const void* dO, const float* LSE,
+                     float* dQ, float* dK, float* dV, int B, int H, int H_kv, int N, int d, float scale, int causal,
+                     const int32_t* kv_len, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Merge of attention results over disjoint key sets (split-KV or sequence-parallel attention: each
  * part attends the same queries to its own keys). For every row,
  *     LSE = log(sum_i exp(LSE_i)),   O = sum_i exp(LSE_i - LSE) O_i
