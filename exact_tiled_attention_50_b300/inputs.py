@@ -125,3 +125,26 @@ def custom(B: int, H: int, H_kv: int, N: int, d: int, dtype: str = "bf16", *, ca
     if kv_len is not None:
         x.kv_len = torch.as_tensor(kv_len, dtype=torch.int32).reshape(B)
     return x
+
+
+def random_signs(d: int, seed: int = 0) -> torch.Tensor:
+    """d random signs (int8, +-1): the random draw of the fp8 path's rotation, passed to it as an input.
+    Drawn as ``randint(0, 2, (d,))`` from a generator seeded ``SEED_BASE + 2000 + seed``; 0 -> -1."""
+    g = torch.Generator("cpu")
+    g.manual_seed(SEED_BASE + 2000 + seed)
+    return (torch.randint(0, 2, (d,), generator=g) * 2 - 1).to(torch.int8)
+
+
+def with_outlier_channels(x: Inputs, n_channels: int = 4, factor: float = 16.0, seed: int = 0) -> Inputs:
+    """The same inputs with ``n_channels`` channels of Q and K (the same channels in both, drawn as
+    ``randperm(d)[:n_channels]`` from a generator seeded ``SEED_BASE + 3000 + seed``) multiplied by
+    ``factor`` (a power of two, so exact in bf16): the large-magnitude feature channels that make
+    per-tile low-precision scales coarse for every other channel."""
+    d = x.q.shape[-1]
+    g = torch.Generator("cpu")
+    g.manual_seed(SEED_BASE + 3000 + seed)
+    ch = torch.randperm(d, generator=g)[:n_channels]
+    q, k = x.q.clone(), x.k.clone()
+    q[..., ch] = q[..., ch] * factor
+    k[..., ch] = k[..., ch] * factor
+    return Inputs(q.contiguous(), k.contiguous(), x.v, x.kv_len, x.scale, x.causal)

@@ -121,3 +121,109 @@ def attention_bwd_np(q, k, v, dO, scale, causal=False, kv_len=None):
             dQ[b, h] = float(scale) * (dS @ k[b, kh])
             dK[b, kh] += float(scale) * (dS.T @ q[b, h])
     return dQ, dK, dV
+
+
+# ------------------------------------------------------------------------------------------------
+# fp8 forward with incoherent processing (section "闪电注意力-3" of "闪电注意力：革命性地提高Transformer
+# 效率", unite.ai: FP8 computation, and a processing step that lowers the quantisation error of the
+# low-precision format). The pages name the two steps without defining them; the reading taken here:
+#   1. rotate Q and K by the same orthogonal matrix, (1/sqrt d) H_d diag(s), H_d the Sylvester
+#      Hadamard matrix and s a caller-supplied vector of random signs; Q K^T is unchanged, and an
+#      outlier channel is spread over all d channels before rounding;
+#   2. round Q, K and V to the 8-bit floating-point format E4M3 with one power-of-two scale per tile
+#      of 128 rows;
+#   3. exact attention over the rounded values.
+# The rotation is applied unnormalised (H_d diag(s)); the factor 1/d of the two rotations moves into
+# the softmax scale. Rounding decisions are taken in fp32, the precision in which the rotated values
+# exist, with the butterflies in the order of the fast transform below.
+# ------------------------------------------------------------------------------------------------
+E4M3_MAX = 448.0
+FP8_TILE_ROWS = 128
+
+
+def e4m3_round(x):
+    """Nearest value of the E4M3 format (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+    subnormals below 2^-6 with spacing 2^-9; largest finite 448; no infinities), ties to even, values
+    beyond the largest finite one clamped to +-448. Returns fp64 values on that grid."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))       # a = f * 2^ex, f in [0.5, 1): binade 2^(ex - 1)
+    e = np.clip(ex - 1, -6, 8)                        # normal binades 2^-6 .. 2^8; below: subnormal spacing
+    step = np.ldexp(1.0, (e - 3).astype(np.int64))    # 3 mantissa bits
+    r = np.round(a / step) * step                     # numpy rounds halves to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.where(x < 0, -r, r)
+
+
+def fwht_f32(x):
+    """Unnormalised Walsh-Hadamard transform (Sylvester order) along the last axis, in fp32: spans
+    h = 1, 2, 4, ...; for each pair (i, i + h) with bit h of i clear, (x_i, x_i+h) <- (x_i + x_i+h,
+    x_i - x_i+h), every output one rounded fp32 addition or subtraction."""
+    y = np.array(x, dtype=np.float32, copy=True)
+    n = y.shape[-1]
+    assert n & (n - 1) == 0
+    lead = y.shape[:-1]
+    h = 1
+    while h < n:
+        z = y.reshape(*lead, n // (2 * h), 2, h)
+        a = z[..., 0, :].copy()
+        b = z[..., 1, :].copy()
+        z[..., 0, :] = a + b
+        z[..., 1, :] = a - b
+        y = z.reshape(*lead, n)
+        h *= 2
+    return y
+
+
+def tile_exponent(x32):
+    """Power-of-two scale 2^e of one tile (any shape, fp32): with e8 the biased fp32 exponent field of
+    the tile's largest |x| (so that max |x| < 2^(e8 - 126)), e = max(e8 - 134, -100): the tile's values
+    times 2^-e stay below 2^8 = 256, inside the E4M3 range. An all-zero tile gets e = 0."""
+    m = np.float32(np.max(np.abs(np.asarray(x32, dtype=np.float32)))) if np.size(x32) else np.float32(0)
+    if m == 0:
+        return 0
+    e8 = int((np.array(m, dtype=np.float32).view(np.uint32) >> 23) & 0xFF)
+    return max(e8 - 134, -100)
+
+
+def quantize_e4m3_tiles(x32, rows=FP8_TILE_ROWS):
+    """x [..., N, d] fp32 -> (dequantised values fp64, exponents [..., ceil(N / rows)]): each tile of
+    `rows` rows is rounded as e4m3_round(x * 2^-e) and stands for that times 2^e."""
+    x32 = np.asarray(x32, dtype=np.float32)
+    N = x32.shape[-2]
+    nt = (N + rows - 1) // rows
+    lead = x32.shape[:-2]
+    out = np.zeros(x32.shape, np.float64)
+    ex = np.zeros(lead + (nt,), np.int64)
+    for idx in np.ndindex(*lead):
+        for t in range(nt):
+            tile = x32[idx][t * rows:(t + 1) * rows]
+            e = tile_exponent(tile)
+            ex[idx + (t,)] = e
+            out[idx][t * rows:(t + 1) * rows] = e4m3_round(tile.astype(np.float64) * 2.0 ** -e) * 2.0 ** e
+    return out, ex
+
+
+def attention_fp8_np(q, k, v, scale, signs=None, causal=False, kv_len=None, return_p=False):
+    """Attention over E4M3-rounded inputs after the optional rotation (steps 1-3 above), fp64.
+
+    q [B,H,N,d], k/v [B,H_kv,N,d] (their values read as fp32), signs: None (no rotation) or d values
+    +-1. Returns O, LSE (and P), computed by the exact definition of ``attention_np`` on the rounded
+    values, plus a dict with the rounded tensors and the tile exponents."""
+    q32 = np.asarray(q, dtype=np.float32)
+    k32 = np.asarray(k, dtype=np.float32)
+    v32 = np.asarray(v, dtype=np.float32)
+    d = q32.shape[-1]
+    sc = float(scale)
+    if signs is not None:
+        s = np.asarray(signs, dtype=np.float32).reshape(d)
+        assert np.all(np.abs(s) == 1)
+        q32 = fwht_f32(q32 * s)
+        k32 = fwht_f32(k32 * s)
+        sc = sc / d
+    qd, eq = quantize_e4m3_tiles(q32)
+    kd, ek = quantize_e4m3_tiles(k32)
+    vd, ev = quantize_e4m3_tiles(v32)
+    res = attention_np(qd, kd, vd, sc, causal=causal, kv_len=kv_len, return_p=return_p)
+    parts = dict(q=qd, k=kd, v=vd, eq=eq, ek=ek, ev=ev, scale=sc)
+    return (*res, parts)
