@@ -20,7 +20,8 @@ ATTN_F32, ATTN_BF16 = 0, 1
 EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_workspace_bytes", "attn_launches_per_call",
             "attn_debug_set_wait_limit_ns", "attn_debug_set_skip_kv_load", "attn_set_kernel_events",
             "attn_event_elapsed_ms", "attn_fwd_noalloc", "attn_debug_schedule",
-            "attn_debug_last_error_bits", "attn_merge", "attn_bwd", "attn_bwd_workspace_bytes")
+            "attn_debug_last_error_bits", "attn_merge", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_fp8",
+            "attn_fwd_fp8_workspace_bytes")
 
 
 class AttnError(RuntimeError):
@@ -41,6 +42,10 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd_noalloc.restype = ci
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, vp, sz, vp]
     lib.attn_bwd.restype = ci
+    lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, vp, vp, sz, vp]
+    lib.attn_fwd_fp8.restype = ci
+    lib.attn_fwd_fp8_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
+    lib.attn_fwd_fp8_workspace_bytes.restype = sz
     lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
     lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_merge.argtypes = [vp, vp, ci, ctypes.c_longlong, ci, vp, vp, vp]
@@ -137,6 +142,40 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
                       workspace.numel() * workspace.element_size() if workspace is not None else 0, stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[float] = None,
+                 causal: bool = False, kv_len: Optional[torch.Tensor] = None, signs: Optional[torch.Tensor] = None,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None):
+    """O, LSE of the fp8 path (E4M3 tensor cores; Q, K rotated by the random signs `signs` (int8 [d],
+    +-1, on the device) or not rotated when None). q, k, v bf16 CUDA tensors, d = 128; O, LSE fp32."""
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if not (q.dtype == k.dtype == v.dtype == torch.bfloat16):
+        raise TypeError("attn_fwd_fp8 takes bf16 q, k, v")
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if kv_len is not None:
+        kv_len = kv_len.to(device=q.device, dtype=torch.int32).contiguous()
+    if signs is not None:
+        signs = signs.to(device=q.device, dtype=torch.int8).contiguous()
+    nbytes = int(lib.attn_fwd_fp8_workspace_bytes(B, H, H_kv, N, d))
+    if workspace is None:
+        workspace = _workspace(max(nbytes, 256), q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, H_kv, N, d,
+                          float(scale), int(bool(causal)), kv_len.data_ptr() if kv_len is not None else None,
+                          signs.data_ptr() if signs is not None else None, workspace.data_ptr(),
+                          workspace.numel() * workspace.element_size(), stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8")
     return out, lse
 
 

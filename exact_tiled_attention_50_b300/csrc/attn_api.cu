@@ -60,6 +60,29 @@ bool workspace_layout(int B, int H_kv, int N, int d, WorkspaceLayout* w) {
     return heads < 65535;  // the pre-pass grid has heads + 1 rows of blocks
 }
 
+// fp8 path: E4M3 copies of Q, K and V^T, their tile exponents, then the schedule's buffers.
+struct Fp8Layout {
+    size_t q8 = 0, k8 = 0, vt8 = 0, qexp = 0, kexp = 0, vexp = 0, boff = 0, flags = 0, part = 0, total = 0;
+    int n_ktiles = 0;
+};
+
+bool fp8_layout(int B, int H, int H_kv, int N, int d, Fp8Layout* w) {
+    const size_t hq = static_cast<size_t>(B) * H, hkv = static_cast<size_t>(B) * H_kv;
+    w->n_ktiles = (N + 127) / 128;
+    const size_t npad = static_cast<size_t>(w->n_ktiles) * 128;
+    w->q8 = 0;
+    w->k8 = round_up(hq * N * d, 256);
+    w->vt8 = w->k8 + round_up(hkv * N * d, 256);
+    w->qexp = w->vt8 + round_up(hkv * d * npad, 256);
+    w->kexp = w->qexp + round_up(hq * w->n_ktiles * sizeof(int32_t), 256);
+    w->vexp = w->kexp + round_up(hkv * w->n_ktiles * sizeof(int32_t), 256);
+    w->boff = w->vexp + round_up(hkv * w->n_ktiles * sizeof(int32_t), 256);
+    w->flags = w->boff + round_up(static_cast<size_t>(B + 1) * sizeof(long long), 256);
+    w->part = w->flags + round_up(8 * attn_impl::SCHED_MAX_CTAS * sizeof(unsigned int), 256);
+    w->total = w->part + round_up(static_cast<size_t>(attn_impl::SCHED_MAX_CTAS) * 2 * (d + 3) * 128 * sizeof(float), 256);
+    return hq + 2 * hkv + 1 <= 65535;  // rows of the pre-pass grid
+}
+
 // SM count of the current device (cached per device).
 int device_sms() {
     static std::atomic<int> cache[64];
@@ -103,6 +126,19 @@ bool encode_out_map(CUtensorMap* m, void* base, int d, int rows, long long slabs
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map over [slabs, rows, inner] bytes (E4M3): box of 128 bytes x 128 rows, 128-byte swizzle, rows
+// past `rows` read as zero.
+bool encode_u8_map(CUtensorMap* m, const void* base, int inner, int rows, long long slabs) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(slabs)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows) * inner};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Tensor maps depend only on (base address, element type, d, rows, slabs, kind), so a small cache
 // keyed on those saves re-encoding them for buffers used again (the common case).
 struct MapKey {
@@ -123,10 +159,11 @@ MapEntry g_map_cache[kMapCache];
 int g_map_next = 0;
 std::mutex g_map_mutex;
 
-enum { MAP_Q_BF16 = 0, MAP_K_BF16 = 1, MAP_V_F16 = 2, MAP_O_F32 = 3 };
+enum { MAP_Q_BF16 = 0, MAP_K_BF16 = 1, MAP_V_F16 = 2, MAP_O_F32 = 3, MAP_U8 = 4 };
 
 bool encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int d, int rows, long long slabs);
 bool encode_out_map(CUtensorMap* m, void* base, int d, int rows, long long slabs);
+bool encode_u8_map(CUtensorMap* m, const void* base, int inner, int rows, long long slabs);
 
 bool get_map(CUtensorMap* m, int kind, const void* base, int d, int rows, long long slabs) {
     const MapKey key{base, kind, d, rows, slabs};
@@ -140,6 +177,7 @@ bool get_map(CUtensorMap* m, int kind, const void* base, int d, int rows, long l
     }
     bool ok = false;
     if (kind == MAP_O_F32) ok = encode_out_map(m, const_cast<void*>(base), d, rows, slabs);
+    else if (kind == MAP_U8) ok = encode_u8_map(m, base, d, rows, slabs);
     else ok = encode_rows_map(m, base, kind == MAP_V_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                               d, rows, slabs);
     if (!ok) return false;
@@ -257,6 +295,92 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     if (timed && cudaEventRecord(ev0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn_impl::launch_attn_tc(d, out_dtype == ATTN_BF16, tmQ, tmK, tmV, tmO, p, stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
+    if (timed && cudaEventRecord(ev1, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+size_t attn_fwd_fp8_workspace_bytes(int B, int H, int H_kv, int N, int d) {
+    if (!sizes_ok(B, H, H_kv, N, d) || d != 128) return 0;
+    Fp8Layout w;
+    if (!fp8_layout(B, H, H_kv, N, d, &w)) return 0;
+    return w.total;
+}
+
+attn_status attn_fwd_fp8(const void* Q, const void* K, const void* V, float* O, float* LSE, int B, int H, int H_kv,
+                         int N, int d, float scale, int causal, const int32_t* kv_len, const int8_t* signs,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!Q || !K || !V || !O) return ATTN_ERR_INVALID_ARG;
+    if (!sizes_ok(B, H, H_kv, N, d)) return ATTN_ERR_INVALID_ARG;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return ATTN_ERR_INVALID_ARG;
+    if (LSE && !aligned(LSE, 4)) return ATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return ATTN_ERR_INVALID_ARG;
+    Fp8Layout w;
+    if (!fp8_layout(B, H, H_kv, N, d, &w)) return ATTN_ERR_UNSUPPORTED;
+    if (attn_impl::plan_max_steps(B, H, N, causal) >= 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total) return ATTN_ERR_INVALID_ARG;
+    if (!get_encoder()) return ATTN_ERR_CUDA;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    attn_impl::Fp8PrepParams fp{};
+    fp.Q = Q;
+    fp.K = K;
+    fp.V = V;
+    fp.Q8 = ws + w.q8;
+    fp.K8 = ws + w.k8;
+    fp.V8T = ws + w.vt8;
+    fp.q_exp = reinterpret_cast<int32_t*>(ws + w.qexp);
+    fp.k_exp = reinterpret_cast<int32_t*>(ws + w.kexp);
+    fp.v_exp = reinterpret_cast<int32_t*>(ws + w.vexp);
+    fp.signs = signs;
+    fp.N = N;
+    fp.d = d;
+    fp.n_ktiles = w.n_ktiles;
+    fp.heads_q = B * H;
+    fp.heads_kv = B * H_kv;
+
+    const int npad = w.n_ktiles * 128;
+    CUtensorMap tmQ, tmK, tmV, tmO;
+    if (!get_map(&tmQ, MAP_U8, fp.Q8, d, N, static_cast<long long>(B) * H) ||
+        !get_map(&tmK, MAP_U8, fp.K8, d, N, static_cast<long long>(B) * H_kv) ||
+        !get_map(&tmV, MAP_U8, fp.V8T, npad, d, static_cast<long long>(B) * H_kv) ||
+        !get_map(&tmO, MAP_O_F32, O, d, N, static_cast<long long>(B) * H))
+        return ATTN_ERR_UNSUPPORTED;
+
+    const int sms = device_sms();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    attn_impl::TcParams p{};
+    p.O = O;
+    p.LSE = LSE;
+    p.kv_len = kv_len;
+    p.v_exp = fp.v_exp;
+    p.q_exp = fp.q_exp;
+    p.k_exp = fp.k_exp;
+    p.n_ktiles = w.n_ktiles;
+    p.boff = reinterpret_cast<const long long*>(ws + w.boff);
+    p.part = reinterpret_cast<float*>(ws + w.part);
+    p.flags = reinterpret_cast<unsigned int*>(ws + w.flags);
+    p.plan = attn_impl::make_plan(B, H, N, causal, kv_len != nullptr, sms);
+    p.H_kv = H_kv;
+    p.group = H / H_kv;
+    // the two unnormalised rotations multiply every score by d (a power of two here)
+    p.scale_log2 = scale * 1.4426950408889634f / (signs ? static_cast<float>(d) : 1.0f);
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.debug_skip_kv_load = g_skip_kv_load.load();
+
+    attn_impl::PlanParams pl{};
+    pl.kv_len = kv_len;
+    pl.boff = reinterpret_cast<long long*>(ws + w.boff);
+    pl.flags = p.flags;
+    pl.B = B; pl.H = H; pl.N = N; pl.n_pairs = p.plan.n_pairs; pl.causal = causal;
+
+    if (attn_impl::launch_fp8_prep(fp, pl, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
+    const bool timed = ev0 && ev1;
+    if (timed && cudaEventRecord(ev0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (attn_impl::launch_attn_tc_fp8(tmQ, tmK, tmV, tmO, p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
     if (timed && cudaEventRecord(ev1, stream) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
 }

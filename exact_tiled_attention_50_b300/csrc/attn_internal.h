@@ -198,6 +198,25 @@ struct TcParams {
     float scale_log2;         // scale * log2(e)
     unsigned long long wait_limit_ns;
     int debug_skip_kv_load;
+    // fp8 path only: power-of-two exponents of the E4M3 copies of Q ([B*H][n_ktiles]) and K
+    // ([B*H_kv][n_ktiles]); a tile's stored values times 2^e are the (rotated) inputs
+    const int32_t* q_exp;
+    const int32_t* k_exp;
+};
+
+// fp8 pre-pass: rotate Q and K (optional), round Q, K, V to E4M3 per 128-row tile, V transposed.
+struct Fp8PrepParams {
+    const void* Q;            // bf16 [B*H][N][d]
+    const void* K;            // bf16 [B*H_kv][N][d]
+    const void* V;            // bf16 [B*H_kv][N][d]
+    uint8_t* Q8;              // E4M3 [B*H][N][d]
+    uint8_t* K8;              // E4M3 [B*H_kv][N][d]
+    uint8_t* V8T;             // E4M3 [B*H_kv][d][n_ktiles * 128] (keys past N are zero)
+    int32_t* q_exp;           // [B*H][n_ktiles]
+    int32_t* k_exp;           // [B*H_kv][n_ktiles]
+    int32_t* v_exp;           // [B*H_kv][n_ktiles]
+    const int8_t* signs;      // d values +-1 (rotation), or nullptr (no rotation)
+    int N, d, n_ktiles, heads_q, heads_kv;
 };
 
 struct PlanParams {
@@ -228,6 +247,10 @@ struct VPrepParams {
 };
 
 cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStream_t stream);
+cudaError_t launch_fp8_prep(const Fp8PrepParams& p, const PlanParams& plan, cudaStream_t stream);
+// fp8 forward (d = 128, fp32 output): maps over Q8, K8 (box 128 x 128 bytes) and V8T (keys inner)
+cudaError_t launch_attn_tc_fp8(const CUtensorMap& tmQ8, const CUtensorMap& tmK8, const CUtensorMap& tmVT8,
+                               const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream);
 // tmO: fp32 output map (box 32 columns x 32 rows, 128-byte swizzle); unused for bf16 output.
 cudaError_t launch_attn_tc(int d, bool out_bf16, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmV16, const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream);

@@ -30,6 +30,14 @@
 // 0-63, 64-127) so that the first four P V k-steps overlap the second half's exponentials.
 // V enters the P V product as fp16 (a per-head power-of-two scale keeps it in range); Q K^T is
 // bf16 x bf16 with fp32 accumulation.
+//
+// fp8 variant (FP8 = true, d = 128; section "闪电注意力-3" of the unite.ai page: FP8 computation with
+// a processing step that lowers the quantisation error): a pre-pass rotates Q and K by the same
+// random-sign Hadamard matrix (Q K^T unchanged) and rounds Q, K and V to E4M3 with one power-of-two
+// scale per 128-row tile; V is stored transposed (keys innermost) so that both products read K-major
+// operands. Both products run as kind::f8f6f4 (E4M3 x E4M3, fp32 accumulation); the softmax folds
+// the tiles' scales into its per-tile multiplier and writes P as E4M3 (four per TMEM column). The
+// lazy-rescale threshold drops to 2^8 so that P stays below the E4M3 maximum 448.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -82,9 +90,6 @@ constexpr int NUM_THREADS = 384;          // 3 warpgroups
 constexpr int MMA_WARP = 8;
 constexpr int TMA_WARP = 9;                // key/value ring producer
 constexpr int QLOAD_WARP = 10;             // query tile producer
-// Lazy rescale: a row keeps its reference maximum until a tile's maximum exceeds it by more than
-// 2^15 (log2 units); exponentials then stay <= 2^15, inside the fp16 range of P (65504).
-constexpr float RESCALE_THRESHOLD = 15.0f;
 constexpr uint32_t TMEM_COLS = 512;
 // Register split: the block launches with 384 x 168 = 64512 registers; the two softmax
 // warpgroups raise theirs to 200 and the MMA/TMA warpgroup lowers its to 104:
@@ -95,19 +100,30 @@ constexpr uint32_t SOFTMAX_REGS = 200;
 constexpr uint32_t CONTROL_REGS = 104;
 static_assert(2 * 128 * SOFTMAX_REGS + 128 * CONTROL_REGS <= NUM_THREADS * LAUNCH_REGS, "register split");
 
-template <int D>
+template <int D, bool FP8>
 struct Cfg {
-    static constexpr int NB = D / 64;                 // 64-element (128-byte) boxes per row
-    static constexpr int TILE_BYTES = NB * 16384;     // one 128 x D tile of 16-bit values
+    static_assert(!FP8 || D == 128, "the fp8 path has d = 128 (one 128-byte row per tile row)");
+    static constexpr int BOX_ELEMS = FP8 ? 128 : 64;  // elements per 128-byte box row
+    static constexpr int NB = D / BOX_ELEMS;          // boxes per tile row
+    static constexpr int TILE_BYTES = NB * 16384;     // one 128 x D tile (fp8: also the 128 x 128 V^T tile)
     // Shared memory: Q_0, Q_1, the segment's first key tile K_k0, then NP ring stages of
     // (V_j, K_j+1), consumed together (one wait and one release per key step).
-    static constexpr int NP = (D == 128) ? 2 : 4;
+    static constexpr int NP = (D == 128 && !FP8) ? 2 : 4;
+    // S = Q K^T k-steps: 16 bf16 or 32 E4M3 elements, 32 bytes of each row either way
+    static constexpr int KSTEPS = FP8 ? D / 32 : D / 16;
+    // Lazy rescale: a row keeps its reference maximum until a tile's maximum exceeds it by more than
+    // this (log2 units); exponentials then stay <= 2^15, inside the fp16 range of P (65504), or
+    // <= 2^8, inside the E4M3 range (448).
+    static constexpr float RESCALE_THRESHOLD = FP8 ? 8.0f : 15.0f;
     static constexpr int OFF_K0 = 2 * TILE_BYTES;
     static constexpr int OFF_RING = 3 * TILE_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // V slot then K slot
     static constexpr int SMEM_BYTES = 1024 + OFF_RING + NP * STAGE_BYTES;
-    static constexpr uint32_t IDESC_S = idesc_f16(BLOCK_M, BLOCK_N, 1, 1, 0, 0);  // bf16, K-major both
-    static constexpr uint32_t IDESC_O = idesc_f16(BLOCK_M, D, 0, 0, 0, 1);        // f16, B (V) MN-major
+    // bf16 S: K-major both; f16 P V: B (V) MN-major. fp8: E4M3 everywhere, every operand K-major
+    // (V^T tile: d rows of 128 keys).
+    static constexpr uint32_t IDESC_S = FP8 ? idesc_f8f6f4(BLOCK_M, BLOCK_N, 0, 0, 0, 0)
+                                            : idesc_f16(BLOCK_M, BLOCK_N, 1, 1, 0, 0);
+    static constexpr uint32_t IDESC_O = FP8 ? idesc_f8f6f4(BLOCK_M, D, 0, 0, 0, 0) : idesc_f16(BLOCK_M, D, 0, 0, 0, 1);
     static constexpr uint32_t TMEM_O = 256;
     // epilogue staging buffers (4 KB each) per softmax warp inside its tile's Q region
     static constexpr int EPI_BUFS = TILE_BYTES / 4 / 4096;
@@ -164,12 +180,12 @@ __device__ __forceinline__ SegInfo seg_info(const TcParams& p, const Segment& s)
     return si;
 }
 
-template <int D, bool OUT_BF16>
+template <int D, bool OUT_BF16, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                        const __grid_constant__ TcParams p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -264,7 +280,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_arrive_expect_tx(&bar_k0_full, C::TILE_BYTES);
                     if (!skip_k)
                         for (int bx = 0; bx < C::NB; ++bx)
-                            tma_load_3d_hint(smem + C::OFF_K0 + bx * 16384, &tmK, &bar_k0_full, bx * 64,
+                            tma_load_3d_hint(smem + C::OFF_K0 + bx * 16384, &tmK, &bar_k0_full, bx * C::BOX_ELEMS,
                                              s.k0 * BLOCK_N, si.zkv, pol_kv);
                     skip_k = false;
                     ++segk;
@@ -280,13 +296,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const bool has_k = j + 1 < jend;
                         mbar_arrive_expect_tx(&bar_full[st], has_k ? 2 * C::TILE_BYTES : C::TILE_BYTES);
                         uint8_t* dst = smem + C::OFF_RING + st * C::STAGE_BYTES;
-                        for (int bx = 0; bx < C::NB; ++bx)
-                            tma_load_3d_hint(dst + bx * 16384, &tmV, &bar_full[st], bx * 64, j * BLOCK_N, si.zkv,
-                                             pol_kv);
+                        if constexpr (FP8) {  // V^T tile: keys j*128.. (innermost), all d rows
+                            tma_load_3d_hint(dst, &tmV, &bar_full[st], j * BLOCK_N, 0, si.zkv, pol_kv);
+                        } else {
+                            for (int bx = 0; bx < C::NB; ++bx)
+                                tma_load_3d_hint(dst + bx * 16384, &tmV, &bar_full[st], bx * 64, j * BLOCK_N, si.zkv,
+                                                 pol_kv);
+                        }
                         if (has_k)
                             for (int bx = 0; bx < C::NB; ++bx)
-                                tma_load_3d_hint(dst + C::TILE_BYTES + bx * 16384, &tmK, &bar_full[st], bx * 64,
-                                                 (j + 1) * BLOCK_N, si.zkv, pol_kv);
+                                tma_load_3d_hint(dst + C::TILE_BYTES + bx * 16384, &tmK, &bar_full[st],
+                                                 bx * C::BOX_ELEMS, (j + 1) * BLOCK_N, si.zkv, pol_kv);
                         ++g;
                     }
                 }
@@ -328,8 +348,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int t = 0; t < 2; ++t)
                         if (si.n[t] > 0)
                             for (int bx = 0; bx < C::NB; ++bx)
-                                tma_load_3d_hint(smem + t * C::TILE_BYTES + bx * 16384, &tmQ, &bar_q, bx * 64,
-                                                 si.q0[t], si.bh, pol_q);
+                                tma_load_3d_hint(smem + t * C::TILE_BYTES + bx * 16384, &tmQ, &bar_q,
+                                                 bx * C::BOX_ELEMS, si.q0[t], si.bh, pol_q);
                     ++segq;
                 }
                 if (!ok || abort_flag) {
@@ -351,25 +371,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t dQ = sdesc_sw128(smem_u32(smem), 16, 1024);
             const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::OFF_K0), 16, 1024);
             const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING + C::TILE_BYTES), 16, 1024);
-            const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16384, 1024);
+            // V: MN-major fp16 tile (keys x d), or, fp8, the K-major V^T tile (d rows x 128 keys)
+            const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), FP8 ? 16 : 16384, 1024);
             auto issue_S = [&](int t, uint64_t dk) {
                 const uint64_t a = dQ + static_cast<uint64_t>((t * C::TILE_BYTES) >> 4);
                 const uint32_t d = tmem + t * BLOCK_N;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
                     const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    umma_ss(d, a + off, dk + off, C::IDESC_S, kk > 0);
+                    if constexpr (FP8) umma_ss_f8(d, a + off, dk + off, C::IDESC_S, kk > 0);
+                    else umma_ss(d, a + off, dk + off, C::IDESC_S, kk > 0);
                 }
             };
-            // P V over keys [64*half, 64*half + 64): four k-steps of 16 keys
+            // P V over keys [64*half, 64*half + 64): four k-steps of 16 keys (fp16 P, 2 per TMEM
+            // column), or two of 32 keys (E4M3 P, 4 per column); 8 columns per k-step either way
             auto issue_PV_half = [&](int t, uint64_t dv, int half, bool accumulate) {
                 const uint32_t d = tmem + C::TMEM_O + t * D;
                 const uint32_t a = tmem + t * BLOCK_N;
+                if constexpr (FP8) {
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int kk = half * 4 + k4;
-                    umma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_O,
-                            (accumulate || kk > 0));
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        const int kk = half * 2 + k2;
+                        umma_ts_f8(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 32) >> 4), C::IDESC_O,
+                                   (accumulate || kk > 0));
+                    }
+                } else {
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const int kk = half * 4 + k4;
+                        umma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_O,
+                                (accumulate || kk > 0));
+                    }
                 }
             };
             const Segment& s = seg_sh[MMA_WARP];
@@ -505,6 +537,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // per-tile exponents of the fp16 V copy; this piece's O holds sum P V * 2^-E with E the
             // largest exponent of the tiles seen so far (the same for every row of the tile)
             const int32_t* vexp_row = p.v_exp + static_cast<size_t>(s.b * p.H_kv + s.h / p.group) * p.n_ktiles;
+            // fp8: the stored Q and K tiles stand for their values times 2^eq and 2^ek, so a score is
+            // the tensor-core sum times 2^(eq + ek); both go into the multiplier of this tile
+            float sl_t = sl;
+            const int32_t* kexp_row = nullptr;
+            if constexpr (FP8) {
+                kexp_row = p.k_exp + static_cast<size_t>(s.b * p.H_kv + s.h / p.group) * p.n_ktiles;
+                if (q0t < p.plan.N)
+                    sl_t = ldexpf(sl, __ldg(p.q_exp + static_cast<size_t>(s.b * p.plan.H + s.h) * p.n_ktiles +
+                                            q0t / BLOCK_M));
+            }
             int E = 0;
             float m_run = -INFINITY;                   // reference maximum (log2 domain, already scaled)
             float l_run = 0.f;                         // running sum of exp2(s*sl - m_run)
@@ -512,6 +554,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int jj = 0; jj < nkvt; ++jj) {
                 const int j = k0 + jj;
                 const int e_j = __ldg(vexp_row + j);
+                float slj = sl;
+                if constexpr (FP8) slj = ldexpf(sl_t, __ldg(kexp_row + j));
                 // tcgen05.ld/st below are warp-collective: the warp proceeds only if every lane's wait
                 // succeeded
                 if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s, 0);
@@ -549,23 +593,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int i = 0; i < 128; ++i)
                         if (i >= lim) x[i] = -INFINITY;
                 }
-                // row maximum: four independent chains of three-input maxima
+                // row maximum: four independent chains of three-input maxima over x[4..123], then
+                // the last four values
                 float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-                for (int i = 4; i < 128; i += 8) {
+                for (int i = 4; i < 124; i += 8) {
                     mx0 = max3f(mx0, x[i], x[i + 1]);
                     mx1 = max3f(mx1, x[i + 2], x[i + 3]);
                     mx2 = max3f(mx2, x[i + 4], x[i + 5]);
                     mx3 = max3f(mx3, x[i + 6], x[i + 7]);
                 }
-                const float m_tile = max3f(mx0, mx1, fmaxf(mx2, mx3)) * sl;
+                mx0 = max3f(mx0, x[124], x[125]);
+                mx1 = max3f(mx1, x[126], x[127]);
+                const float m_tile = max3f(mx0, mx1, fmaxf(mx2, mx3)) * slj;
                 float alpha = 1.f;
                 bool rescale = false;
                 if (jj == 0) {
                     m_run = m_tile;
                     E = e_j;
                 } else {
-                    if (m_tile > m_run + RESCALE_THRESHOLD) {
+                    if (m_tile > m_run + C::RESCALE_THRESHOLD) {
                         alpha = ex2_approx(m_run - m_tile);
                         l_run *= alpha;
                         m_run = m_tile;
@@ -607,26 +654,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // sum takes P itself.
                 {
                     const int shift = e_j - E;  // <= 0, almost always 0
-                    const f32x2 sl2 = make_f32x2(sl, sl);
+                    const f32x2 sl2 = make_f32x2(slj, slj);
                     const f32x2 nm2 = make_f32x2(static_cast<float>(shift) - m_sub, static_cast<float>(shift) - m_sub);
                     f32x2 acc0 = make_f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        uint32_t pk[32];
+                        if constexpr (FP8) {
+                            // E4M3, four keys per TMEM column: 16 columns per half
+                            uint32_t pk[16];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            float e0, e1;
-                            split_f32x2(
-                                fma_f32x2(make_f32x2(x[64 * half + 2 * i], x[64 * half + 2 * i + 1]), sl2, nm2), e0,
-                                e1);
-                            e0 = ex2_approx(e0);
-                            e1 = ex2_approx(e1);
-                            const f32x2 e = make_f32x2(e0, e1);
-                            if (i & 1) acc1 = add_f32x2(acc1, e);
-                            else acc0 = add_f32x2(acc0, e);
-                            pk[i] = pack_f16x2(e0, e1);
+                            for (int i = 0; i < 16; ++i) {
+                                float e0, e1, e2, e3;
+                                const int c0 = 64 * half + 4 * i;
+                                split_f32x2(fma_f32x2(make_f32x2(x[c0], x[c0 + 1]), sl2, nm2), e0, e1);
+                                split_f32x2(fma_f32x2(make_f32x2(x[c0 + 2], x[c0 + 3]), sl2, nm2), e2, e3);
+                                e0 = ex2_approx(e0);
+                                e1 = ex2_approx(e1);
+                                e2 = ex2_approx(e2);
+                                e3 = ex2_approx(e3);
+                                acc0 = add_f32x2(acc0, make_f32x2(e0, e1));
+                                acc1 = add_f32x2(acc1, make_f32x2(e2, e3));
+                                pk[i] = pack_e4m3x4(e0, e1, e2, e3);
+                            }
+                            tmem_st16(tS + 16 * half, pk);
+                        } else {
+                            uint32_t pk[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                float e0, e1;
+                                split_f32x2(
+                                    fma_f32x2(make_f32x2(x[64 * half + 2 * i], x[64 * half + 2 * i + 1]), sl2, nm2),
+                                    e0, e1);
+                                e0 = ex2_approx(e0);
+                                e1 = ex2_approx(e1);
+                                const f32x2 e = make_f32x2(e0, e1);
+                                if (i & 1) acc1 = add_f32x2(acc1, e);
+                                else acc0 = add_f32x2(acc0, e);
+                                pk[i] = pack_f16x2(e0, e1);
+                            }
+                            tmem_st32(tS + 32 * half, pk);
                         }
-                        tmem_st32(tS + 32 * half, pk);
                         tmem_wait_st();
                         tc_fence_before();
                         mbar_arrive(&bar_p_full[t][half]);
@@ -965,10 +1032,165 @@ cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStrea
     return cudaGetLastError();
 }
 
-template <int D, bool OUT_BF16>
+// ---------------------------------------------------------------------------------------------
+// fp8 pre-pass (d = 128): one block per 128-row tile of Q, K or V, plus the plan block.
+// Q and K rows are multiplied by the signs and transformed by the unnormalised Walsh-Hadamard
+// butterflies (spans 1, 2 inside a lane, 4 .. 64 across lanes; each output one fp32 addition or
+// subtraction, in that order), then every tile is rounded to E4M3 at its own power-of-two scale.
+// ---------------------------------------------------------------------------------------------
+constexpr int FP8P_THREADS = 256;
+
+// Tile exponent from the largest |x| as fp32 bits: max |x| < 2^(e8 - 126); e = max(e8 - 134, -100)
+// keeps the tile's values times 2^-e below 256 = 2^8 (E4M3 holds up to 448); a zero tile gets 0.
+__device__ __forceinline__ int fp8_tile_exponent(uint32_t max_abs_bits) {
+    if (max_abs_bits == 0) return 0;
+    const int e8 = static_cast<int>((max_abs_bits >> 23) & 0xffu);
+    return max(e8 - 134, -100);
+}
+
+// Block-wide maximum of non-negative fp32 bit patterns (their order is that of the values).
+__device__ __forceinline__ uint32_t fp8_block_max(uint32_t v, uint32_t* red) {
+    v = __reduce_max_sync(0xffffffffu, v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < FP8P_THREADS / 32; ++i) m = max(m, red[i]);
+    return m;
+}
+
+// 2^-e as fp32 for e in [-100, 120]
+__device__ __forceinline__ float fp8_pow2_neg(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
+
+// One 128-row tile of Q or K: warp w holds rows 16w .. 16w+15, lane l elements 4l .. 4l+3.
+__device__ void fp8_prep_qk_tile(const __nv_bfloat16* src, uint8_t* dst, int32_t* exp_out, const int8_t* signs,
+                                 int N, int tile, uint32_t* red) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float sg[4] = {1.f, 1.f, 1.f, 1.f};
+    if (signs) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sg[c] = static_cast<float>(__ldg(signs + 4 * lane + c));
+    }
+    float v[16][4];
+    uint32_t mbits = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int row = tile * 128 + warp * 16 + i;
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+        if (row < N) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + static_cast<size_t>(row) * 128) + lane);
+            a[0] = __uint_as_float(u.x << 16);
+            a[1] = __uint_as_float(u.x & 0xffff0000u);
+            a[2] = __uint_as_float(u.y << 16);
+            a[3] = __uint_as_float(u.y & 0xffff0000u);
+        }
+        if (signs) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) a[c] *= sg[c];
+            const float b0 = a[0] + a[1], b1 = a[0] - a[1], b2 = a[2] + a[3], b3 = a[2] - a[3];
+            a[0] = b0 + b2;
+            a[2] = b0 - b2;
+            a[1] = b1 + b3;
+            a[3] = b1 - b3;
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float o = __shfl_xor_sync(0xffffffffu, a[c], m);
+                    a[c] = (lane & m) ? o - a[c] : a[c] + o;
+                }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            v[i][c] = a[c];
+            mbits = max(mbits, __float_as_uint(a[c]) & 0x7fffffffu);
+        }
+    }
+    const int e = fp8_tile_exponent(fp8_block_max(mbits, red));
+    if (threadIdx.x == 0) *exp_out = e;
+    const float sc = fp8_pow2_neg(e);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int row = tile * 128 + warp * 16 + i;
+        if (row < N)
+            reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(row) * 128)[lane] =
+                pack_e4m3x4(v[i][0] * sc, v[i][1] * sc, v[i][2] * sc, v[i][3] * sc);
+    }
+}
+
+// One 128-key tile of V, rounded and written transposed: dst row c (dimension c) holds the tile's
+// 128 keys at columns tile*128 ..; keys past N are zero.
+__device__ void fp8_prep_v_tile(const __nv_bfloat16* src, uint8_t* dstT, int32_t* exp_out, int N, int n_cols,
+                                int tile, uint32_t* red, uint16_t (*sm)[130]) {
+    uint32_t mbits = 0;  // largest |V| as bf16 bits
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int idx = threadIdx.x + k * FP8P_THREADS;  // 16-byte vector of the tile: row idx/16
+        const int row = idx >> 4, c8 = (idx & 15) * 8;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (tile * 128 + row < N)
+            u = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(tile * 128 + row) * 128) + (idx & 15));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            sm[row][c8 + 2 * q] = static_cast<uint16_t>(w[q] & 0xffffu);
+            sm[row][c8 + 2 * q + 1] = static_cast<uint16_t>(w[q] >> 16);
+            mbits = max(mbits, max(w[q] & 0x7fffu, (w[q] >> 16) & 0x7fffu));
+        }
+    }
+    const int e = fp8_tile_exponent(fp8_block_max(mbits << 16, red));  // (the reduction synchronises sm)
+    if (threadIdx.x == 0) *exp_out = e;
+    const float sc = fp8_pow2_neg(e);
+    const int c = threadIdx.x >> 1, k0 = (threadIdx.x & 1) * 64;
+    uint32_t o[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        float f[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) f[u] = __uint_as_float(static_cast<uint32_t>(sm[k0 + 4 * q + u][c]) << 16) * sc;
+        o[q] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(dstT + static_cast<size_t>(c) * n_cols + tile * 128 + k0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+
+__global__ void __launch_bounds__(FP8P_THREADS) fp8_prep_kernel(const Fp8PrepParams p, const PlanParams pl) {
+    __shared__ uint32_t red[FP8P_THREADS / 32];
+    __shared__ uint16_t vt[128][130];
+    const int tile = blockIdx.x, y = blockIdx.y;
+    const size_t head_elems = static_cast<size_t>(p.N) * 128;
+    if (y < p.heads_q) {
+        fp8_prep_qk_tile(static_cast<const __nv_bfloat16*>(p.Q) + y * head_elems, p.Q8 + y * head_elems,
+                         p.q_exp + static_cast<size_t>(y) * p.n_ktiles + tile, p.signs, p.N, tile, red);
+    } else if (y < p.heads_q + p.heads_kv) {
+        const int h = y - p.heads_q;
+        fp8_prep_qk_tile(static_cast<const __nv_bfloat16*>(p.K) + h * head_elems, p.K8 + h * head_elems,
+                         p.k_exp + static_cast<size_t>(h) * p.n_ktiles + tile, p.signs, p.N, tile, red);
+    } else if (y < p.heads_q + 2 * p.heads_kv) {
+        const int h = y - p.heads_q - p.heads_kv;
+        const int n_cols = p.n_ktiles * 128;
+        fp8_prep_v_tile(static_cast<const __nv_bfloat16*>(p.V) + h * head_elems,
+                        p.V8T + static_cast<size_t>(h) * 128 * n_cols, p.v_exp + static_cast<size_t>(h) * p.n_ktiles + tile,
+                        p.N, n_cols, tile, red, vt);
+    } else if (tile == 0) {
+        plan_block(pl);
+    }
+}
+
+cudaError_t launch_fp8_prep(const Fp8PrepParams& p, const PlanParams& plan, cudaStream_t stream) {
+    if (p.d != 128) return cudaErrorInvalidValue;
+    const long long rows = static_cast<long long>(p.heads_q) + 2LL * p.heads_kv + 1;
+    if (rows > 65535) return cudaErrorInvalidConfiguration;
+    fp8_prep_kernel<<<dim3(p.n_ktiles, static_cast<unsigned>(rows)), FP8P_THREADS, 0, stream>>>(p, plan);
+    return cudaGetLastError();
+}
+
+template <int D, bool OUT_BF16, bool FP8>
 static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
-    auto kern = attn_fwd_tc_kernel<D, OUT_BF16>;
+    auto kern = attn_fwd_tc_kernel<D, OUT_BF16, FP8>;
     cudaError_t e = cudaSuccess;
     // once per device: shared-memory opt-in and the register check
     static std::atomic<int> ready[64];
@@ -976,7 +1198,7 @@ static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, c
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || ready[dev].load(std::memory_order_acquire) == 0) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, FP8>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         // The register split inside the kernel assumes exactly LAUNCH_REGS registers per thread at
         // launch; with fewer, the softmax warpgroups' increase could never be granted.
@@ -992,7 +1214,7 @@ static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, c
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.plan.G));
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = Cfg<D>::SMEM_BYTES;
+    cfg.dynamicSmemBytes = Cfg<D, FP8>::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -1006,11 +1228,16 @@ static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, c
 
 cudaError_t launch_attn_tc(int d, bool out_bf16, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmV16, const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
-    if (d == 128) return out_bf16 ? launch_tc_t<128, true>(tmQ, tmK, tmV16, tmO, p, stream)
-                                  : launch_tc_t<128, false>(tmQ, tmK, tmV16, tmO, p, stream);
-    if (d == 64) return out_bf16 ? launch_tc_t<64, true>(tmQ, tmK, tmV16, tmO, p, stream)
-                                 : launch_tc_t<64, false>(tmQ, tmK, tmV16, tmO, p, stream);
+    if (d == 128) return out_bf16 ? launch_tc_t<128, true, false>(tmQ, tmK, tmV16, tmO, p, stream)
+                                  : launch_tc_t<128, false, false>(tmQ, tmK, tmV16, tmO, p, stream);
+    if (d == 64) return out_bf16 ? launch_tc_t<64, true, false>(tmQ, tmK, tmV16, tmO, p, stream)
+                                 : launch_tc_t<64, false, false>(tmQ, tmK, tmV16, tmO, p, stream);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_tc_fp8(const CUtensorMap& tmQ8, const CUtensorMap& tmK8, const CUtensorMap& tmVT8,
+                               const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
+    return launch_tc_t<128, false, true>(tmQ8, tmK8, tmVT8, tmO, p, stream);
 }
 
 #ifdef ATTN_TRACE

@@ -91,6 +91,36 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
                      attn_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fp8 attention forward with incoherent processing (section "闪电注意力-3" of the unite.ai page names
+ * FP8 computation and a processing step that lowers the quantisation error of the low-precision
+ * format; this library reads the step as a random orthogonal rotation of Q and K, which leaves
+ * Q K^T unchanged and spreads an outlier channel over all channels before rounding):
+ *   1. if `signs` is not NULL, every row of Q and K is multiplied elementwise by signs (d values
+ *      +-1, the rotation's random draw, chosen by the caller) and transformed by the Walsh-Hadamard
+ *      matrix H_d (unnormalised; the factor 1/d of the two transforms moves into the score scale);
+ *   2. Q, K and V are rounded to E4M3 (OCP 8-bit float: 4 exponent bits, 3 mantissa bits, max 448;
+ *      round to nearest even, saturating) with one power-of-two scale per 128-row tile per head,
+ *      2^e with e = max(e8 - 134, -100) for the largest |x| of the tile having fp32 exponent field e8;
+ *   3. the attention of attn_fwd over the rounded values, both products on the E4M3 tensor cores
+ *      with fp32 accumulation; the probabilities P enter P V as E4M3 as well.
+ * Result: the attention of the rounded inputs, up to the E4M3 rounding of P (relative 2^-4 per
+ * probability) and fp32 arithmetic. Not exact attention: the rounding of the inputs is part of it.
+ *   Q, K, V      device bf16 pointers, [B, H, N, d] / [B, H_kv, N, d] as for attn_fwd
+ *   O, LSE       device fp32 [B, H, N, d] and [B, H, N] (LSE may be NULL)
+ *   d            128 only (other values: ATTN_ERR_UNSUPPORTED)
+ *   scale, causal, kv_len, stream   as for attn_fwd
+ *   signs        device int8 [d] with values +1 / -1, or NULL (no rotation)
+ *   workspace    device, attn_fwd_fp8_workspace_bytes() bytes, 256-byte aligned: the E4M3 copies
+ *                of Q, K and V (V transposed), their tile exponents, the work schedule and the
+ *                partial results of split work units; scratch between calls
+ * Errors as attn_fwd; timeouts of bounded waits are reported by attn_check.
+ */
+size_t attn_fwd_fp8_workspace_bytes(int B, int H, int H_kv, int N, int d);
+attn_status attn_fwd_fp8(const void* Q, const void* K, const void* V, float* O, float* LSE, int B, int H, int H_kv,
+                         int N, int d, float scale, int causal, const int32_t* kv_len, const int8_t* signs,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Backward pass of attn_fwd (bf16 inputs): the gradients of the output O with respect to Q, K and V
  * for an upstream gradient dO. The pages state the forward only; this is its chain rule in the
  * recompute form of "闪电注意力：革命性地提高Transformer效率" (unite.ai: the attention matrix is not

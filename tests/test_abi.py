@@ -83,3 +83,31 @@ def test_merge_invalid_arguments(lib, bad):
 
 def test_unsupported_combination(lib):
     assert _call(lib, ind=0, outd=1) == lib.ATTN_ERR_UNSUPPORTED
+
+
+def test_fp8_workspace_bytes(lib):
+    w = lib.lib.attn_fwd_fp8_workspace_bytes(2, 8, 2, 1000, 128)
+    # E4M3 copies of Q (B H N d), K (B H_kv N d), V^T (B H_kv d N padded to 128) at least
+    assert w >= 2 * 8 * 1000 * 128 + 2 * 2 * 1000 * 128 + 2 * 2 * 128 * 1024 and w % 256 == 0
+    assert lib.lib.attn_fwd_fp8_workspace_bytes(2, 8, 2, 1000, 64) == 0  # d = 128 only
+    assert lib.lib.attn_fwd_fp8_workspace_bytes(2, 8, 3, 1000, 128) == 0
+
+
+def _call_fp8(lib, **kw):
+    a = dict(Q=4096, K=4096, V=4096, O=4096, LSE=None, B=1, H=2, H_kv=1, N=128, d=128, scale=0.125, causal=0,
+             kv_len=None, signs=None, ws=4096, ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.lib.attn_fwd_fp8(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["H_kv"], a["N"],
+                                a["d"], a["scale"], a["causal"], a["kv_len"], a["signs"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(Q=None), dict(O=None), dict(B=0), dict(N=0), dict(H=3, H_kv=2), dict(scale=0.0),
+    dict(scale=float("nan")), dict(causal=3), dict(K=4100), dict(ws=None), dict(ws=4096 + 64), dict(ws_bytes=1000),
+])
+def test_fp8_invalid_arguments_rejected_without_launch(lib, bad):
+    assert _call_fp8(lib, **bad) == lib.ATTN_ERR_INVALID_ARG
+
+
+def test_fp8_head_dim_other_than_128_unsupported(lib):
+    assert _call_fp8(lib, d=64) == lib.ATTN_ERR_UNSUPPORTED

@@ -56,6 +56,19 @@ def test_peaky_sweep_n2048_full():
     parity.check_full(x, "bf16", what="sweep n2048 causal (full)")
 
 
+# ---------------------------------------------------------------- rows whose scores are all far below 0
+@pytest.mark.parametrize("N", [1, 3, 200])
+@pytest.mark.parametrize("d", [64, 128])
+def test_rows_with_only_negative_scores(N, d):
+    """Q shifted by +2 and K by -2 in every channel: every score is about -4 d scale (about -45 for
+    d = 128), the softmax is still well defined. The running maximum must be the row's own (a larger
+    reference, such as 0, would underflow every fp16 probability: O = 0)."""
+    x = inputs.custom(1, 2, 1, N, d, causal=True, seed=90 + N)
+    x.q = (x.q.float() + 2.0).to(torch.bfloat16).contiguous()
+    x.k = (x.k.float() - 2.0).to(torch.bfloat16).contiguous()
+    parity.check_full(x, "bf16", what=f"negative scores N={N} d={d}")
+
+
 # ---------------------------------------------------------------- edges: ragged sizes, masks, heads
 @pytest.mark.parametrize("N", [1, 2, 100, 127, 128, 129, 200, 255, 256, 257, 384, 513])
 @pytest.mark.parametrize("d", [64, 128])
