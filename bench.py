@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 from exact_tiled_attention_50_b300 import inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s and % of B300 dense-BF16 peak at N=8192, d=128"
+METRIC_FP8 = "attention fwd TFLOP/s of the fp8 (E4M3) path and % of B300 dense-FP8 peak at N=8192, d=128"
 UNIT = "TFLOP/s"
 # query rows of the fp64 oracle: the CPU-baseline leg times CPU_ROWS rows (10-30 s on the host cores);
 # the reference arm spreads about REF_BUDGET_ROWS rows over all of its steps
@@ -131,10 +132,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(w):
+def profiled_traffic(w, path_kind="bf16"):
     """DRAM bytes per launch of the attention kernel from the committed ncu summary of this workload,
     or None when there is none or the kernel source changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"attn_fwd_tc_kernel_b{w.B}h{w.H}_n{w.N}_d{w.d}.md")
+    tag = "_fp8" if path_kind == "fp8" else ""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_tc_kernel{tag}_b{w.B}h{w.H}_n{w.N}_d{w.d}.md")
     if not os.path.exists(path):
         return None
     kv = {}
@@ -210,13 +212,22 @@ def run_ours(args, w):
     B, H, N, d = q.shape
     out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    wsb = attn.workspace_bytes(B, w.H, w.H_kv, N, d, q.dtype)
+    fp8 = args.path == "fp8"
+    if fp8:
+        wsb = int(attn.lib.attn_fwd_fp8_workspace_bytes(B, w.H, w.H_kv, N, d))
+        signs = inputs.random_signs(d, seed=0).to(dev)
+    else:
+        wsb = attn.workspace_bytes(B, w.H, w.H_kv, N, d, q.dtype)
     work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        attn.attn_fwd(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, out=out, lse=lse, workspace=work)
+        if fp8:
+            attn.attn_fwd_fp8(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, signs=signs, out=out, lse=lse,
+                              workspace=work)
+        else:
+            attn.attn_fwd(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, out=out, lse=lse, workspace=work)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -294,23 +305,30 @@ def run_ours(args, w):
     flops = flops_of(w)
     peaks = load_peaks()
     achieved = flops / (kern_ms * 1e-3) / 1e12
+    # the contraction's own dtype: E4M3 takes the measured bf16 peak times the nominal fp8 / bf16 ratio
+    # (4.5 / 2.25 PFLOP/s dense)
+    peak = peaks["bf16"] * (2.0 if fp8 else 1.0)
+    peak_sus = peaks["bf16_sustained"] * (2.0 if fp8 else 1.0)
     line = {
-        "metric": METRIC,
+        "metric": METRIC_FP8 if fp8 else METRIC,
         "value": ws * flops / (step_ms * 1e-3) / 1e12,
         "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1), 1% of key rows x8)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d, "causal": w.causal,
                    "in": "bf16", "out": "fp32 O + fp32 LSE",
+                   "path": "fp8: Q, K rotated (random signs) + E4M3 per 128-row tile; E4M3 tensor cores"
+                           if fp8 else "bf16 tensor cores (fp16 P, fp16 V)",
                    "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
                    "parallelism": f"replicas x{ws} (independent problems per GPU)",
                    "pct_of_peak_bf16": 100.0 * flops / (step_ms * 1e-3) / 1e12 / peaks["bf16"]},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": UNIT,
-                     "frac": achieved / peaks["bf16"],
-                     "traffic": args.traffic if args.traffic is not None else profiled_traffic(w),
-                     "kernel": "attn_fwd_tc_kernel<128,false>", "kernel_ms": kern_ms,
-                     "peak_source": f"{peaks['source']} bf16 burst (cuBLAS); "
-                                    f"frac of sustained {achieved / peaks['bf16_sustained']:.3f}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak,
+                     "traffic": args.traffic if args.traffic is not None else profiled_traffic(w, args.path),
+                     "kernel": f"attn_fwd_tc_kernel<{w.d},false,{'true' if fp8 else 'false'}>", "kernel_ms": kern_ms,
+                     "peak_source": (f"{peaks['source']} bf16 burst (cuBLAS) x 2 (nominal fp8/bf16 dense ratio)"
+                                     if fp8 else f"{peaks['source']} bf16 burst (cuBLAS)")
+                                    + f"; frac of sustained {achieved / peak_sus:.3f}"},
         "e2e": {"value": ws * flops / (e2e * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
         "gpu_launches": K * attn.launches_per_call(q.dtype),
@@ -340,6 +358,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--traffic", type=float, default=None, help="DRAM bytes per launch from an ncu capture")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["bf16", "fp8"], default="bf16",
+                    help="bf16 tensor-core path (the headline) or the fp8 path with incoherent processing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
