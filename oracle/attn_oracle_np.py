@@ -227,3 +227,101 @@ def attention_fp8_np(q, k, v, scale, signs=None, causal=False, kv_len=None, retu
     res = attention_np(qd, kd, vd, sc, causal=causal, kv_len=kv_len, return_p=return_p)
     parts = dict(q=qd, k=kd, v=vd, eq=eq, ek=ek, ev=ev, scale=sc)
     return (*res, parts)
+
+
+# ------------------------------------------------------------------------------------------------
+# Additive bias and dropout (the xFormers call of the EfficientAttention module on "AI训练的最大障碍
+# 不是算力,而是'内存墙'" (zsdodo.com): memory-efficient attention with attn_bias and a dropout
+# probability p). Reading taken: the bias is added to the scaled scores, the softmax is taken over
+# them (LSE likewise, without dropout), and every probability is kept with probability 1 - p and
+# then divided by that keep probability (inverted dropout) before P V.
+# The keep decisions come from the counter-based generator Philox4x32-10 of Salmon, Moraes, Dror and
+# Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC 2011), so that any tiling reproduces them:
+#   counter (j >> 3, i, b * H + h, offset), key (seed mod 2^32, seed >> 32) for query row i and key j;
+#   the four 32-bit output words give eight 16-bit values u_0..u_7 (word w: low half u_2w, high half
+#   u_2w+1); key j takes u_(j mod 8) and is dropped iff u < t, t = floor(p * 65536). The effective
+#   drop probability is t / 65536 and kept values are scaled by 65536 / (65536 - t).
+# ------------------------------------------------------------------------------------------------
+PHILOX_M0, PHILOX_M1 = 0xD2511F53, 0xCD9E8D57        # round multipliers
+PHILOX_W0, PHILOX_W1 = 0x9E3779B9, 0xBB67AE85        # key increments (Weyl sequence)
+_U32 = np.uint64(0xFFFFFFFF)
+
+
+def philox4x32_10(ctr, key):
+    """Philox4x32 with 10 rounds on arrays of counters ([..., 4] uint32) and keys ([..., 2] uint32).
+    One round: (hi0, lo0) = M0 * x0, (hi1, lo1) = M1 * x2 (64-bit products split into 32-bit halves),
+    x <- (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0); the key advances by (W0, W1) after every round."""
+    x = [np.asarray(ctr[..., i], dtype=np.uint64) & _U32 for i in range(4)]
+    k0 = np.asarray(key[..., 0], dtype=np.uint64) & _U32
+    k1 = np.asarray(key[..., 1], dtype=np.uint64) & _U32
+    for _ in range(10):
+        p0 = np.uint64(PHILOX_M0) * x[0]
+        p1 = np.uint64(PHILOX_M1) * x[2]
+        hi0, lo0 = p0 >> np.uint64(32), p0 & _U32
+        hi1, lo1 = p1 >> np.uint64(32), p1 & _U32
+        x = [hi1 ^ x[1] ^ k0, lo1, hi0 ^ x[3] ^ k1, lo0]
+        k0 = (k0 + np.uint64(PHILOX_W0)) & _U32
+        k1 = (k1 + np.uint64(PHILOX_W1)) & _U32
+    return np.stack([a.astype(np.uint32) for a in x], axis=-1)
+
+
+def dropout_threshold(p):
+    """t = floor(p * 65536) for 0 <= p < 1 (p read as the fp32 value the C ABI receives)."""
+    p = float(np.float32(p))
+    assert 0.0 <= p < 1.0
+    return int(np.floor(p * 65536.0))
+
+
+def dropout_keep_mask(B, H, N, p, seed, offset):
+    """Boolean [B, H, N, N]: True where probability (b, h, i, j) is kept (see the section text)."""
+    t = dropout_threshold(p)
+    G = (N + 7) // 8
+    g, i, bh = np.meshgrid(np.arange(G), np.arange(N), np.arange(B * H), indexing="ij")
+    ctr = np.stack([g, i, bh, np.full_like(g, int(offset) & 0xFFFFFFFF)], axis=-1).astype(np.uint64)
+    key = np.broadcast_to(np.array([int(seed) & 0xFFFFFFFF, (int(seed) >> 32) & 0xFFFFFFFF], np.uint64),
+                          ctr.shape[:-1] + (2,))
+    w = philox4x32_10(ctr, key).astype(np.uint32)                      # [G, N, BH, 4]
+    u = np.stack([w & 0xFFFF, w >> 16], axis=-1).reshape(G, N, B * H, 8)  # u_(2w), u_(2w+1)
+    keep = u >= t                                                      # [G, N, BH, 8]
+    keep = np.transpose(keep, (2, 1, 0, 3)).reshape(B * H, N, G * 8)[:, :, :N]
+    return keep.reshape(B, H, N, N)
+
+
+def attention_bias_dropout_np(q, k, v, scale, bias=None, p=0.0, seed=0, offset=0, causal=False, kv_len=None,
+                              return_p=False):
+    """O, LSE of the biased, dropped-out attention (fp64). bias: None or an array broadcastable to
+    [B, H, N, N] (natural-log units, added to scale * Q K^T). LSE is that of the biased scores."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    g = H // H_kv
+    bias_full = np.zeros((B, H, N, N)) if bias is None else np.broadcast_to(np.asarray(bias, dtype=np.float64),
+                                                                              (B, H, N, N))
+    t = dropout_threshold(p)
+    keep = dropout_keep_mask(B, H, N, p, seed, offset) if t > 0 else np.ones((B, H, N, N), bool)
+    inv_keep = 65536.0 / (65536.0 - t)
+    O = np.zeros((B, H, N, d))
+    LSE = np.zeros((B, H, N))
+    P_all = np.zeros((B, H, N, N)) if return_p else None
+    for b in range(B):
+        L = N if kv_len is None else int(kv_len[b])
+        mask = key_mask(N, causal, L)
+        for h in range(H):
+            S = float(scale) * (q[b, h] @ k[b, h // g].T) + bias_full[b, h]
+            S = np.where(mask, S, -np.inf)
+            m = S.max(axis=1)
+            has = np.isfinite(m)
+            m_safe = np.where(has, m, 0.0)
+            E = np.exp(S - m_safe[:, None])
+            l = E.sum(axis=1)
+            P = np.where(has[:, None], E / np.where(has, l, 1.0)[:, None], 0.0)
+            O[b, h] = (P * keep[b, h] * inv_keep) @ v[b, h // g]
+            with np.errstate(divide="ignore"):
+                LSE[b, h] = np.where(has, m_safe + np.log(np.where(has, l, 1.0)), -np.inf)
+            if return_p:
+                P_all[b, h] = P
+    if return_p:
+        return O, LSE, P_all
+    return O, LSE
