@@ -21,7 +21,7 @@ EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_workspace_byte
             "attn_debug_set_wait_limit_ns", "attn_debug_set_skip_kv_load", "attn_set_kernel_events",
             "attn_event_elapsed_ms", "attn_fwd_noalloc", "attn_debug_schedule",
             "attn_debug_last_error_bits", "attn_merge", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_fp8",
-            "attn_fwd_fp8_workspace_bytes")
+            "attn_fwd_fp8_workspace_bytes", "attn_fwd_ex")
 
 
 class AttnError(RuntimeError):
@@ -42,6 +42,10 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd_noalloc.restype = ci
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, vp, sz, vp]
     lib.attn_bwd.restype = ci
+    ll = ctypes.c_longlong
+    lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, vp, ll, ll, ll, cf,
+                                ctypes.c_uint64, ctypes.c_uint32, vp, sz, vp]
+    lib.attn_fwd_ex.restype = ci
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, vp, vp, sz, vp]
     lib.attn_fwd_fp8.restype = ci
     lib.attn_fwd_fp8_workspace_bytes.argtypes = [ci, ci, ci, ci, ci]
@@ -142,6 +146,51 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
                       workspace.numel() * workspace.element_size() if workspace is not None else 0, stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[float] = None,
+                causal: bool = False, kv_len: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
+                dropout_p: float = 0.0, seed: int = 0, offset: int = 0, out: Optional[torch.Tensor] = None,
+                lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """O, LSE of the attention with an additive bias and dropout (bf16 q, k, v; fp32 O, LSE).
+
+    bias: bf16 CUDA tensor broadcastable to [B, H, N, N] whose last dimension is contiguous; broadcast
+    dimensions are passed as zero strides (no copy). The library needs 16-byte aligned rows: strides
+    that are multiples of 8 elements (pad the last dimension when N is not). dropout_p, seed, offset:
+    the dropout probability and the generator's key and counter word (see attn_fwd_ex in attn.h)."""
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if not (q.dtype == k.dtype == v.dtype == torch.bfloat16):
+        raise TypeError("attn_fwd_ex takes bf16 q, k, v")
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if kv_len is not None:
+        kv_len = kv_len.to(device=q.device, dtype=torch.int32).contiguous()
+    strides = (0, 0, 0)
+    if bias is not None:
+        if bias.dtype != torch.bfloat16 or not bias.is_cuda:
+            raise TypeError("bias must be a bf16 CUDA tensor")
+        bias = bias.expand(B, H, N, N)
+        if bias.stride(3) != 1:
+            raise ValueError("the bias's last dimension must be contiguous")
+        strides = (bias.stride(0), bias.stride(1), bias.stride(2))
+    nbytes = workspace_bytes(B, H, H_kv, N, d, q.dtype)
+    if workspace is None:
+        workspace = _workspace(max(nbytes, 256), q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib.attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, H_kv, N, d,
+                         float(scale), int(bool(causal)), kv_len.data_ptr() if kv_len is not None else None,
+                         bias.data_ptr() if bias is not None else None, *strides, float(dropout_p),
+                         int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF, workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_ex")
     return out, lse
 
 

@@ -198,47 +198,12 @@ bool sizes_ok(int B, int H, int H_kv, int N, int d) {
     return true;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t attn_workspace_bytes(int B, int H, int H_kv, int N, int d, attn_dtype in_dtype) {
-    if (!sizes_ok(B, H, H_kv, N, d)) return 0;
-    if (in_dtype != ATTN_BF16) return 0;
-    WorkspaceLayout w;
-    if (!workspace_layout(B, H_kv, N, d, &w)) return 0;
-    return w.total;
-}
-
-attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
-                     int N, int d, float scale, int causal, const int32_t* kv_len, attn_dtype in_dtype,
-                     attn_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    if (!Q || !K || !V || !O) return ATTN_ERR_INVALID_ARG;
-    if (!sizes_ok(B, H, H_kv, N, d)) return ATTN_ERR_INVALID_ARG;
-    if (!(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
-    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return ATTN_ERR_INVALID_ARG;
-    if (LSE && !aligned(LSE, 4)) return ATTN_ERR_INVALID_ARG;
-    if (kv_len && !aligned(kv_len, 4)) return ATTN_ERR_INVALID_ARG;
-    if (in_dtype != ATTN_F32 && in_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
-    if (out_dtype != ATTN_F32 && out_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
-
-    if (in_dtype == ATTN_F32) {
-        if (out_dtype != ATTN_F32) return ATTN_ERR_UNSUPPORTED;
-        if (static_cast<long long>(B) * H > 65535) return ATTN_ERR_UNSUPPORTED;
-        attn_impl::F32Params p{};
-        p.Q = static_cast<const float*>(Q);
-        p.K = static_cast<const float*>(K);
-        p.V = static_cast<const float*>(V);
-        p.O = O;
-        p.LSE = LSE;
-        p.kv_len = kv_len;
-        p.B = B; p.H = H; p.H_kv = H_kv; p.N = N; p.group = H / H_kv; p.causal = causal;
-        p.scale = scale;
-        return attn_impl::launch_attn_f32(d, p, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-    }
-
-    // bf16 inputs: tensor-core path
+// bf16 inputs on the tensor-core path (attn_fwd and attn_fwd_ex): V -> fp16 pre-pass, then the
+// persistent attention kernel; `ex` (bias + dropout) selects that variant of the kernel.
+attn_status run_bf16_path(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
+                          int N, int d, float scale, int causal, const int32_t* kv_len, attn_dtype out_dtype,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                          const attn_impl::TcParams* ex) {
     WorkspaceLayout w;
     if (!workspace_layout(B, H_kv, N, d, &w)) return ATTN_ERR_UNSUPPORTED;
     if (attn_impl::plan_max_steps(B, H, N, causal) >= 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
@@ -282,6 +247,17 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     p.scale_log2 = scale * 1.4426950408889634f;
     p.wait_limit_ns = g_wait_limit_ns.load();
     p.debug_skip_kv_load = g_skip_kv_load.load();
+    if (ex) {
+        p.bias = ex->bias;
+        p.bias_sb = ex->bias_sb;
+        p.bias_sh = ex->bias_sh;
+        p.bias_sr = ex->bias_sr;
+        p.drop_t = ex->drop_t;
+        p.seed_lo = ex->seed_lo;
+        p.seed_hi = ex->seed_hi;
+        p.rng_offset = ex->rng_offset;
+        p.keep_scale = ex->keep_scale;
+    }
 
     attn_impl::PlanParams pl{};
     pl.kv_len = kv_len;
@@ -293,10 +269,88 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
     const bool timed = ev0 && ev1;
     if (timed && cudaEventRecord(ev0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (attn_impl::launch_attn_tc(d, out_dtype == ATTN_BF16, tmQ, tmK, tmV, tmO, p, stream) != cudaSuccess)
-        return ATTN_ERR_CUDA;
+    const cudaError_t le = ex ? attn_impl::launch_attn_tc_ex(d, tmQ, tmK, tmV, tmO, p, stream)
+                              : attn_impl::launch_attn_tc(d, out_dtype == ATTN_BF16, tmQ, tmK, tmV, tmO, p, stream);
+    if (le != cudaSuccess) return ATTN_ERR_CUDA;
     if (timed && cudaEventRecord(ev1, stream) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_workspace_bytes(int B, int H, int H_kv, int N, int d, attn_dtype in_dtype) {
+    if (!sizes_ok(B, H, H_kv, N, d)) return 0;
+    if (in_dtype != ATTN_BF16) return 0;
+    WorkspaceLayout w;
+    if (!workspace_layout(B, H_kv, N, d, &w)) return 0;
+    return w.total;
+}
+
+attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
+                     int N, int d, float scale, int causal, const int32_t* kv_len, attn_dtype in_dtype,
+                     attn_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!Q || !K || !V || !O) return ATTN_ERR_INVALID_ARG;
+    if (!sizes_ok(B, H, H_kv, N, d)) return ATTN_ERR_INVALID_ARG;
+    if (!(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return ATTN_ERR_INVALID_ARG;
+    if (LSE && !aligned(LSE, 4)) return ATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return ATTN_ERR_INVALID_ARG;
+    if (in_dtype != ATTN_F32 && in_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (out_dtype != ATTN_F32 && out_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+
+    if (in_dtype == ATTN_F32) {
+        if (out_dtype != ATTN_F32) return ATTN_ERR_UNSUPPORTED;
+        if (static_cast<long long>(B) * H > 65535) return ATTN_ERR_UNSUPPORTED;
+        attn_impl::F32Params p{};
+        p.Q = static_cast<const float*>(Q);
+        p.K = static_cast<const float*>(K);
+        p.V = static_cast<const float*>(V);
+        p.O = O;
+        p.LSE = LSE;
+        p.kv_len = kv_len;
+        p.B = B; p.H = H; p.H_kv = H_kv; p.N = N; p.group = H / H_kv; p.causal = causal;
+        p.scale = scale;
+        return attn_impl::launch_attn_f32(d, p, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    }
+
+    // bf16 inputs: tensor-core path
+    return run_bf16_path(Q, K, V, O, LSE, B, H, H_kv, N, d, scale, causal, kv_len, out_dtype, workspace,
+                         workspace_bytes, stream, nullptr);
+}
+
+attn_status attn_fwd_ex(const void* Q, const void* K, const void* V, float* O, float* LSE, int B, int H, int H_kv,
+                        int N, int d, float scale, int causal, const int32_t* kv_len, const void* bias,
+                        long long bias_stride_b, long long bias_stride_h, long long bias_stride_row, float dropout_p,
+                        uint64_t seed, uint32_t offset, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!Q || !K || !V || !O) return ATTN_ERR_INVALID_ARG;
+    if (!sizes_ok(B, H, H_kv, N, d)) return ATTN_ERR_INVALID_ARG;
+    if (!(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return ATTN_ERR_INVALID_ARG;
+    if (LSE && !aligned(LSE, 4)) return ATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return ATTN_ERR_INVALID_ARG;
+    if (!(dropout_p >= 0.f && dropout_p < 1.f)) return ATTN_ERR_INVALID_ARG;  // also rejects NaN
+    if (bias) {
+        if (!aligned(bias, 16)) return ATTN_ERR_INVALID_ARG;
+        for (long long st : {bias_stride_b, bias_stride_h, bias_stride_row})
+            if (st < 0 || st % 8 != 0) return ATTN_ERR_INVALID_ARG;
+    }
+    attn_impl::TcParams ex{};
+    ex.bias = static_cast<const uint16_t*>(bias);
+    ex.bias_sb = bias_stride_b;
+    ex.bias_sh = bias_stride_h;
+    ex.bias_sr = bias_stride_row;
+    const double t = floor(static_cast<double>(dropout_p) * 65536.0);
+    ex.drop_t = static_cast<uint32_t>(t);
+    ex.keep_scale = static_cast<float>(65536.0 / (65536.0 - t));
+    ex.seed_lo = static_cast<uint32_t>(seed & 0xffffffffull);
+    ex.seed_hi = static_cast<uint32_t>(seed >> 32);
+    ex.rng_offset = offset;
+    return run_bf16_path(Q, K, V, O, LSE, B, H, H_kv, N, d, scale, causal, kv_len, ATTN_F32, workspace,
+                         workspace_bytes, stream, &ex);
 }
 
 size_t attn_fwd_fp8_workspace_bytes(int B, int H, int H_kv, int N, int d) {

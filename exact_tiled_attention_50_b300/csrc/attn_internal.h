@@ -202,6 +202,14 @@ struct TcParams {
     // ([B*H_kv][n_ktiles]); a tile's stored values times 2^e are the (rotated) inputs
     const int32_t* q_exp;
     const int32_t* k_exp;
+    // bias + dropout variant only: additive bf16 bias (element (b, h, i, j) at
+    // bias[b * bias_sb + h * bias_sh + i * bias_sr + j], strides in elements, multiples of 8) or
+    // nullptr; dropout threshold t (drop iff the 16-bit draw < t; 0 = no dropout), Philox key and
+    // counter word 3, and the inverse keep probability 65536 / (65536 - t)
+    const uint16_t* bias;
+    long long bias_sb, bias_sh, bias_sr;
+    uint32_t drop_t, seed_lo, seed_hi, rng_offset;
+    float keep_scale;
 };
 
 // fp8 pre-pass: rotate Q and K (optional), round Q, K, V to E4M3 per 128-row tile, V transposed.
@@ -249,6 +257,9 @@ struct VPrepParams {
 cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStream_t stream);
 cudaError_t launch_fp8_prep(const Fp8PrepParams& p, const PlanParams& plan, cudaStream_t stream);
 // fp8 forward (d = 128, fp32 output): maps over Q8, K8 (box 128 x 128 bytes) and V8T (keys inner)
+// bias + dropout variant (bf16 inputs, fp32 output, d in {64, 128})
+cudaError_t launch_attn_tc_ex(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV16,
+                              const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream);
 cudaError_t launch_attn_tc_fp8(const CUtensorMap& tmQ8, const CUtensorMap& tmK8, const CUtensorMap& tmVT8,
                                const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream);
 // tmO: fp32 output map (box 32 columns x 32 rows, 128-byte swizzle); unused for bf16 output.

@@ -135,6 +135,21 @@ __device__ __forceinline__ void record_failure(volatile int* abort_flag, uint32_
     atomicOr(&g_attn_error, ERRBIT_TIMEOUT | bits);
 }
 
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2,
+// 3", SC 2011): per round the 64-bit products M0 * x0 and M1 * x2 are split into halves and
+// x <- (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0); the key then advances by (W0, W1).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, x.x), lo0 = 0xD2511F53u * x.x;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, x.z), lo1 = 0xCD9E8D57u * x.z;
+        x = make_uint4(hi1 ^ x.y ^ k0, lo1, hi0 ^ x.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return x;
+}
+
 __device__ __forceinline__ int clamp_len(const int32_t* kv_len, int b, int N) {
     if (!kv_len) return N;
     int L = __ldg(kv_len + b);
@@ -180,11 +195,14 @@ __device__ __forceinline__ SegInfo seg_info(const TcParams& p, const Segment& s)
     return si;
 }
 
-template <int D, bool OUT_BF16, bool FP8>
+// VAR: 0 = bf16 inputs, 1 = fp8 (E4M3) path, 2 = bf16 inputs with additive bias and dropout
+template <int D, bool OUT_BF16, int VAR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                        const __grid_constant__ TcParams p) {
+    constexpr bool FP8 = VAR == 1;
+    constexpr bool EXTRA = VAR == 2;
     using C = Cfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -547,6 +565,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     sl_t = ldexpf(sl, __ldg(p.q_exp + static_cast<size_t>(s.b * p.plan.H + s.h) * p.n_ktiles +
                                             q0t / BLOCK_M));
             }
+            // bias + dropout: this row's bias (nullptr: none, or a row past N) and its Philox counter words
+            const uint16_t* brow = nullptr;
+            if constexpr (EXTRA) {
+                if (p.bias && row < p.plan.N)
+                    brow = p.bias + s.b * p.bias_sb + s.h * p.bias_sh + static_cast<long long>(row) * p.bias_sr;
+            }
             int E = 0;
             float m_run = -INFINITY;                   // reference maximum (log2 domain, already scaled)
             float l_run = 0.f;                         // running sum of exp2(s*sl - m_run)
@@ -556,6 +580,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int e_j = __ldg(vexp_row + j);
                 float slj = sl;
                 if constexpr (FP8) slj = ldexpf(sl_t, __ldg(kexp_row + j));
+                // bias + dropout: this tile's 128 bias values of the row, loaded before the wait for S
+                // so that their latency overlaps it (keys past N read as 0; they are masked anyway)
+                uint4 bv[EXTRA ? 16 : 1];
+                if constexpr (EXTRA) {
+                    const int kb = j * BLOCK_N;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int kc = kb + 8 * c;
+                        if (brow == nullptr) {
+                            bv[c] = make_uint4(0u, 0u, 0u, 0u);
+                        } else if (kc + 8 <= p.plan.N) {
+                            bv[c] = __ldg(reinterpret_cast<const uint4*>(brow + kc));
+                        } else {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const uint32_t lo = kc + 2 * e < p.plan.N ? __ldg(brow + kc + 2 * e) : 0u;
+                                const uint32_t hi = kc + 2 * e + 1 < p.plan.N ? __ldg(brow + kc + 2 * e + 1) : 0u;
+                                w[e] = lo | (hi << 16);
+                            }
+                            bv[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
                 // tcgen05.ld/st below are warp-collective: the warp proceeds only if every lane's wait
                 // succeeded
                 if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s, 0);
@@ -568,24 +616,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 1);
-                uint32_t ra[32], rb[32], rc[32], rd[32];
-                tmem_ld32(tS + 0, ra);
-                tmem_ld32(tS + 32, rb);
-                tmem_ld32(tS + 64, rc);
-                tmem_ld32(tS + 96, rd);
-                tmem_wait_ld(ra);
-                tmem_wait_ld(rb);
-                tmem_wait_ld(rc);
-                tmem_wait_ld(rd);
-                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 2);
                 float x[128];
+                if constexpr (EXTRA) {
+                    // scores to the log2 domain with the bias added: x = S * scale*log2e + bias * log2e,
+                    // in two halves so that the bias registers of a half die before the next half lands
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    x[i] = __uint_as_float(ra[i]);
-                    x[32 + i] = __uint_as_float(rb[i]);
-                    x[64 + i] = __uint_as_float(rc[i]);
-                    x[96 + i] = __uint_as_float(rd[i]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t ra[32], rb[32];
+                        tmem_ld32(tS + 64 * hh, ra);
+                        tmem_ld32(tS + 64 * hh + 32, rb);
+                        tmem_wait_ld(ra);
+                        tmem_wait_ld(rb);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 b4 = bv[8 * hh + c];
+                            const uint32_t w[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int i = 8 * c + 2 * e;  // key within the half
+                                const uint32_t s0 = i < 32 ? ra[i] : rb[i - 32];
+                                const uint32_t s1 = i + 1 < 32 ? ra[i + 1] : rb[i + 1 - 32];
+                                x[64 * hh + i] = fmaf(__uint_as_float(w[e] << 16), 1.4426950408889634f,
+                                                      __uint_as_float(s0) * slj);
+                                x[64 * hh + i + 1] = fmaf(__uint_as_float(w[e] & 0xffff0000u), 1.4426950408889634f,
+                                                          __uint_as_float(s1) * slj);
+                            }
+                        }
+                    }
+                    slj = 1.0f;  // x is already in log2 units
+                } else {
+                    uint32_t ra[32], rb[32], rc[32], rd[32];
+                    tmem_ld32(tS + 0, ra);
+                    tmem_ld32(tS + 32, rb);
+                    tmem_ld32(tS + 64, rc);
+                    tmem_ld32(tS + 96, rd);
+                    tmem_wait_ld(ra);
+                    tmem_wait_ld(rb);
+                    tmem_wait_ld(rc);
+                    tmem_wait_ld(rd);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        x[i] = __uint_as_float(ra[i]);
+                        x[32 + i] = __uint_as_float(rb[i]);
+                        x[64 + i] = __uint_as_float(rc[i]);
+                        x[96 + i] = __uint_as_float(rd[i]);
+                    }
                 }
+                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 2);
                 const int key0 = j * BLOCK_N;
                 if (key0 + BLOCK_N > kv_valid || (p.plan.causal && key0 + BLOCK_N - 1 > q0t)) {
                     const int lim = row_lim - key0;
@@ -679,6 +756,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tmem_st16(tS + 16 * half, pk);
                         } else {
                             uint32_t pk[32];
+                            uint4 rnd = make_uint4(0u, 0u, 0u, 0u);  // dropout draws of 8 keys
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
                                 float e0, e1;
@@ -688,8 +766,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 e0 = ex2_approx(e0);
                                 e1 = ex2_approx(e1);
                                 const f32x2 e = make_f32x2(e0, e1);
-                                if (i & 1) acc1 = add_f32x2(acc1, e);
+                                if (i & 1) acc1 = add_f32x2(acc1, e);  // the row sum takes P before dropout
                                 else acc0 = add_f32x2(acc0, e);
+                                if constexpr (EXTRA) {
+                                    if (p.drop_t != 0u) {
+                                        // keys 2i, 2i+1 of this half: word (i mod 4) of the draws of their
+                                        // group of 8, low half for the even key, high half for the odd one
+                                        if ((i & 3) == 0)
+                                            rnd = philox4x32_10(
+                                                make_uint4(static_cast<uint32_t>((key0 + 64 * half + 2 * i) >> 3),
+                                                           static_cast<uint32_t>(row),
+                                                           static_cast<uint32_t>(s.b * p.plan.H + s.h), p.rng_offset),
+                                                p.seed_lo, p.seed_hi);
+                                        const uint32_t w = (i & 3) == 0 ? rnd.x : (i & 3) == 1 ? rnd.y
+                                                         : (i & 3) == 2 ? rnd.z : rnd.w;
+                                        if ((w & 0xffffu) < p.drop_t) e0 = 0.f;
+                                        if ((w >> 16) < p.drop_t) e1 = 0.f;
+                                    }
+                                }
                                 pk[i] = pack_f16x2(e0, e1);
                             }
                             tmem_st32(tS + 32 * half, pk);
@@ -824,7 +918,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (t == 0 && r == 0) ATTN_SEG_TRACE(seg_no, 9, static_cast<long long>(global_timer_ns()));
             const int bh = s.b * p.plan.H + s.h;
-            const float inv = L > 0.f ? ldexpf(1.0f, Emax) / L : 0.f;
+            float inv = L > 0.f ? ldexpf(1.0f, Emax) / L : 0.f;
+            if constexpr (EXTRA) inv *= p.keep_scale;  // inverted dropout (1 without dropout)
             const bool store = row < p.plan.N;
             const size_t obase = (static_cast<size_t>(bh) * p.plan.N + (store ? row : 0)) * D;
             const uint32_t stage_base = smem_u32(smem + t * C::TILE_BYTES + wq * C::EPI_BUFS * 4096);
@@ -1187,10 +1282,11 @@ cudaError_t launch_fp8_prep(const Fp8PrepParams& p, const PlanParams& plan, cuda
     return cudaGetLastError();
 }
 
-template <int D, bool OUT_BF16, bool FP8>
+template <int D, bool OUT_BF16, int VAR>
 static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
-    auto kern = attn_fwd_tc_kernel<D, OUT_BF16, FP8>;
+    constexpr bool FP8 = VAR == 1;
+    auto kern = attn_fwd_tc_kernel<D, OUT_BF16, VAR>;
     cudaError_t e = cudaSuccess;
     // once per device: shared-memory opt-in and the register check
     static std::atomic<int> ready[64];
@@ -1228,16 +1324,23 @@ static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, c
 
 cudaError_t launch_attn_tc(int d, bool out_bf16, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmV16, const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
-    if (d == 128) return out_bf16 ? launch_tc_t<128, true, false>(tmQ, tmK, tmV16, tmO, p, stream)
-                                  : launch_tc_t<128, false, false>(tmQ, tmK, tmV16, tmO, p, stream);
-    if (d == 64) return out_bf16 ? launch_tc_t<64, true, false>(tmQ, tmK, tmV16, tmO, p, stream)
-                                 : launch_tc_t<64, false, false>(tmQ, tmK, tmV16, tmO, p, stream);
+    if (d == 128) return out_bf16 ? launch_tc_t<128, true, 0>(tmQ, tmK, tmV16, tmO, p, stream)
+                                  : launch_tc_t<128, false, 0>(tmQ, tmK, tmV16, tmO, p, stream);
+    if (d == 64) return out_bf16 ? launch_tc_t<64, true, 0>(tmQ, tmK, tmV16, tmO, p, stream)
+                                 : launch_tc_t<64, false, 0>(tmQ, tmK, tmV16, tmO, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_tc_ex(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV16,
+                              const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
+    if (d == 128) return launch_tc_t<128, false, 2>(tmQ, tmK, tmV16, tmO, p, stream);
+    if (d == 64) return launch_tc_t<64, false, 2>(tmQ, tmK, tmV16, tmO, p, stream);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_tc_fp8(const CUtensorMap& tmQ8, const CUtensorMap& tmK8, const CUtensorMap& tmVT8,
                                const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
-    return launch_tc_t<128, false, true>(tmQ8, tmK8, tmVT8, tmO, p, stream);
+    return launch_tc_t<128, false, 1>(tmQ8, tmK8, tmVT8, tmO, p, stream);
 }
 
 #ifdef ATTN_TRACE

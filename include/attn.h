@@ -91,6 +91,33 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
                      attn_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Attention forward with an additive bias and dropout (bf16 inputs, fp32 output): the interface of
+ * the xFormers memory-efficient attention call in the EfficientAttention module of "AI训练的最大障碍
+ * 不是算力,而是'内存墙'" (zsdodo.com), which passes attn_bias and a dropout probability p. Read as
+ *     s_ij  = scale * q_i . k_j + bias[b,h,i,j]       (masks of attn_fwd applied on top)
+ *     P_ij  = softmax_j(s_ij),   LSE_i = ln sum_j exp(s_ij)      (no dropout in either)
+ *     O_i   = sum_j P_ij keep_ij / (1 - t / 65536) V_j
+ * keep_ij comes from the counter-based generator Philox4x32-10 (Salmon, Moraes, Dror, Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC 2011) with key (seed mod 2^32, seed >> 32)
+ * and counter (j >> 3, i, b * H + h, offset): its output words w0..w3 give eight 16-bit values
+ * u_2m = w_m mod 2^16, u_2m+1 = w_m >> 16, and key j keeps its probability iff u_(j mod 8) >= t,
+ * t = floor(dropout_p * 65536) (effective drop probability t / 65536). Any tiling or schedule draws
+ * the same mask; a different `offset` (or seed) draws an independent one.
+ *   bias       device bf16 or NULL: element (b, h, i, j) at bias[b * stride_b + h * stride_h +
+ *              i * stride_row + j] (strides in elements, >= 0, multiples of 8; 16-byte aligned base;
+ *              a stride of 0 broadcasts, e.g. one [N, N] bias for every batch and head). Values may
+ *              be -inf (masking); the row must hold N valid entries.
+ *   dropout_p  0 <= p < 1 (0: no dropout);  seed, offset: the generator's key and counter word 3
+ *   workspace  attn_workspace_bytes(B, H, H_kv, N, d, ATTN_BF16) bytes, as for attn_fwd
+ * Other arguments, errors and asynchrony as attn_fwd (invalid strides, alignment or p:
+ * ATTN_ERR_INVALID_ARG).
+ */
+attn_status attn_fwd_ex(const void* Q, const void* K, const void* V, float* O, float* LSE, int B, int H, int H_kv,
+                        int N, int d, float scale, int causal, const int32_t* kv_len, const void* bias,
+                        long long bias_stride_b, long long bias_stride_h, long long bias_stride_row, float dropout_p,
+                        uint64_t seed, uint32_t offset, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fp8 attention forward with incoherent processing (section "闪电注意力-3" of the unite.ai page names
  * FP8 computation and a processing step that lowers the quantisation error of the low-precision
  * format; this library reads the step as a random orthogonal rotation of Q and K, which leaves

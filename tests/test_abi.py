@@ -111,3 +111,21 @@ def test_fp8_invalid_arguments_rejected_without_launch(lib, bad):
 
 def test_fp8_head_dim_other_than_128_unsupported(lib):
     assert _call_fp8(lib, d=64) == lib.ATTN_ERR_UNSUPPORTED
+
+
+def _call_ex(lib, **kw):
+    a = dict(Q=4096, K=4096, V=4096, O=4096, LSE=None, B=1, H=2, H_kv=1, N=128, d=64, scale=0.125, causal=0,
+             kv_len=None, bias=None, sb=0, sh=0, sr=128, p=0.1, seed=1, off=0, ws=4096, ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.lib.attn_fwd_ex(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["H_kv"], a["N"], a["d"],
+                               a["scale"], a["causal"], a["kv_len"], a["bias"], a["sb"], a["sh"], a["sr"], a["p"],
+                               a["seed"], a["off"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(Q=None), dict(O=None), dict(N=0), dict(d=96), dict(H=3, H_kv=2), dict(scale=-1.0), dict(causal=5),
+    dict(p=1.0), dict(p=-0.1), dict(p=float("nan")), dict(bias=4100), dict(bias=4096, sr=100),
+    dict(bias=4096, sb=-8), dict(bias=4096, sh=12), dict(ws=None), dict(ws_bytes=64),
+])
+def test_ex_invalid_arguments_rejected_without_launch(lib, bad):
+    assert _call_ex(lib, **bad) == lib.ATTN_ERR_INVALID_ARG
