@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 from exact_tiled_attention_50_b300 import inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s and % of B300 dense-BF16 peak at N=8192, d=128"
+METRIC_EX = "attention fwd TFLOP/s with additive bias and/or dropout p=0.1 at N=8192, d=128"
 METRIC_FP8 = "attention fwd TFLOP/s of the fp8 (E4M3) path and % of B300 dense-FP8 peak at N=8192, d=128"
 UNIT = "TFLOP/s"
 # query rows of the fp64 oracle: the CPU-baseline leg times CPU_ROWS rows (10-30 s on the host cores);
@@ -135,7 +136,7 @@ def kernel_source_hash() -> str:
 def profiled_traffic(w, path_kind="bf16"):
     """DRAM bytes per launch of the attention kernel from the committed ncu summary of this workload,
     or None when there is none or the kernel source changed since it was taken."""
-    tag = "_fp8" if path_kind == "fp8" else ""
+    tag = "" if path_kind == "bf16" else "_" + path_kind
     path = os.path.join(ROOT, "profiles", f"attn_fwd_tc_kernel{tag}_b{w.B}h{w.H}_n{w.N}_d{w.d}.md")
     if not os.path.exists(path):
         return None
@@ -213,11 +214,17 @@ def run_ours(args, w):
     out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     fp8 = args.path == "fp8"
+    ex = args.path in ("bias_dropout", "dropout")
+    bias = None
     if fp8:
         wsb = int(attn.lib.attn_fwd_fp8_workspace_bytes(B, w.H, w.H_kv, N, d))
         signs = inputs.random_signs(d, seed=0).to(dev)
     else:
         wsb = attn.workspace_bytes(B, w.H, w.H_kv, N, d, q.dtype)
+    if args.path == "bias_dropout":  # one bf16 bias value per (b, h, i, j), drawn on the device
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(inputs.SEED_BASE + 4000)
+        bias = torch.randn((B, w.H, N, N), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
     work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -226,6 +233,9 @@ def run_ours(args, w):
         if fp8:
             attn.attn_fwd_fp8(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, signs=signs, out=out, lse=lse,
                               workspace=work)
+        elif ex:
+            attn.attn_fwd_ex(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, bias=bias, dropout_p=0.1, seed=1,
+                             offset=0, out=out, lse=lse, workspace=work)
         else:
             attn.attn_fwd(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, out=out, lse=lse, workspace=work)
 
@@ -309,26 +319,37 @@ def run_ours(args, w):
     # (4.5 / 2.25 PFLOP/s dense)
     peak = peaks["bf16"] * (2.0 if fp8 else 1.0)
     peak_sus = peaks["bf16_sustained"] * (2.0 if fp8 else 1.0)
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak}
+    if bias is not None:
+        # the bias (2 B per score) outweighs the tensor work at these sizes: the kernel is HBM-bound
+        nbytes = (bias.numel() * 2 + (q.numel() + k.numel() + v.numel()) * 2 + out.numel() * 4 + lse.numel() * 4)
+        gbs = nbytes / (kern_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                "algorithmic_bytes": nbytes, "tensor_tflops": achieved}
     line = {
-        "metric": METRIC_FP8 if fp8 else METRIC,
+        "metric": {"fp8": METRIC_FP8, "bias_dropout": METRIC_EX, "dropout": METRIC_EX}.get(args.path, METRIC),
         "value": ws * flops / (step_ms * 1e-3) / 1e12,
         "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1), 1% of key rows x8)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d, "causal": w.causal,
                    "in": "bf16", "out": "fp32 O + fp32 LSE",
-                   "path": "fp8: Q, K rotated (random signs) + E4M3 per 128-row tile; E4M3 tensor cores"
-                           if fp8 else "bf16 tensor cores (fp16 P, fp16 V)",
+                   "path": {"fp8": "fp8: Q, K rotated (random signs) + E4M3 per 128-row tile; E4M3 tensor cores",
+                            "bias_dropout": "bf16 + additive bf16 bias [B,H,N,N] + dropout p=0.1 (Philox4x32-10)",
+                            "dropout": "bf16 + dropout p=0.1 (Philox4x32-10)"}.get(args.path,
+                                                                                  "bf16 tensor cores (fp16 P, fp16 V)"),
                    "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
+                   **({"bias": "bf16 [B,H,N,N] resident on the device (not part of the e2e copies)"}
+                      if bias is not None else {}),
                    "parallelism": f"replicas x{ws} (independent problems per GPU)",
                    "pct_of_peak_bf16": 100.0 * flops / (step_ms * 1e-3) / 1e12 / peaks["bf16"]},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak,
+        "roofline": {**roof,
                      "traffic": args.traffic if args.traffic is not None else profiled_traffic(w, args.path),
-                     "kernel": f"attn_fwd_tc_kernel<{w.d},false,{'true' if fp8 else 'false'}>", "kernel_ms": kern_ms,
+                     "kernel": f"attn_fwd_tc_kernel<{w.d},false,{1 if fp8 else 2 if ex else 0}>", "kernel_ms": kern_ms,
                      "peak_source": (f"{peaks['source']} bf16 burst (cuBLAS) x 2 (nominal fp8/bf16 dense ratio)"
-                                     if fp8 else f"{peaks['source']} bf16 burst (cuBLAS)")
-                                    + f"; frac of sustained {achieved / peak_sus:.3f}"},
+                                     if fp8 else f"{peaks['source']} " + ("copy bandwidth" if bias is not None
+                                                                          else "bf16 burst (cuBLAS)"))
+                                    + f"; tensor frac of sustained {achieved / peak_sus:.3f}"},
         "e2e": {"value": ws * flops / (e2e * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
         "gpu_launches": K * attn.launches_per_call(q.dtype),
@@ -358,7 +379,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--traffic", type=float, default=None, help="DRAM bytes per launch from an ncu capture")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["bf16", "fp8"], default="bf16",
+    ap.add_argument("--path", choices=["bf16", "fp8", "bias_dropout", "dropout"], default="bf16",
                     help="bf16 tensor-core path (the headline) or the fp8 path with incoherent processing")
     args = ap.parse_args()
     if args.warmup < 3:
