@@ -12,8 +12,8 @@
 //   MMA warp      S^T = K_j Q_i^T, dP^T = V_j dO_i^T         (TMEM cols 0-127, 128-255)
 //   warps 0-3     one key row each: P^T, dS^T -> bf16 in shared memory (128-byte swizzled)
 //   MMA warp      dV += P^T dO_i, dK += dS^T Q_i, dQ_i = dS K_j   (dQ in cols 0-127)
-//   warps 4-7     one query row each: dQ_i scaled and atomically added into the fp32 dQ in device
-//                 memory (several key tiles add into the same rows)
+//   warps 4-7     one query row each: dQ_i scaled, staged in shared memory and added into the fp32 dQ
+//                 in device memory by bulk tensor reductions (several key tiles add into the same rows)
 //   warp 9        TMA loads (K_j, V_j once; Q_i, dO_i and the row statistics per tile)
 // All waits are bounded as in the forward kernel; a wait that runs out records an error bit.
 #include <cuda.h>
@@ -50,7 +50,8 @@ struct BwCfg {
     static constexpr int OFF_PT = 4 * TILE;   // P^T  [128 keys][128 queries] bf16
     static constexpr int OFF_DST = OFF_PT + 32768;  // dS^T [128 keys][128 queries] bf16
     static constexpr int OFF_STAT = OFF_DST + 32768;  // lse2[128], dvec[128]
-    static constexpr int SMEM = 1024 + OFF_STAT + 1024;
+    static constexpr int OFF_DQS = OFF_STAT + 1024;   // dQ staging: 4 warps x (32 rows x 32 fp32), swizzled
+    static constexpr int SMEM = 1024 + OFF_DQS + 4 * 4096;
     static constexpr uint32_t IDESC_SD = idesc_f16(128, 128, 1, 1, 0, 0);  // S^T, dP^T: K-major A and B
     static constexpr uint32_t IDESC_KV = idesc_f16(128, D, 1, 1, 0, 1);    // dV, dK: A K-major, B MN-major
     static constexpr uint32_t IDESC_Q = idesc_f16(128, D, 1, 1, 1, 1);     // dQ: A (dS) and B (K) MN-major
@@ -311,10 +312,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             }
         }
     } else if (warp < 8) {
-        // ======= warps 4-7: one query row each; dQ_i scaled and atomically added into device memory =======
-        // (several key tiles add into the same dQ rows; fp32 reductions at L2, no bulk-group waits)
+        // ===== warps 4-7: one query row each; dQ_i scaled and added into device memory by the tensor =====
+        // store engine (bulk reduce-add of 32 x 32 fp32 boxes staged in shared memory; several key
+        // tiles add into the same dQ rows, the reductions happen at L2)
         const int wq = warp & 3;
         const uint32_t lane_off = tmem_lane_base(wq);
+        const uint32_t stage = smem_u32(smem + C::OFF_DQS + wq * 4096);
         bool ok = true;
         for (int s = 0; s < n_steps && ok; ++s) {
             const bool got = mbar_wait(&bar_dq_full, s & 1, limit_ns, &abort_flag);
@@ -325,8 +328,6 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             }
             tc_fence_after();
             const int bh = b * p.H + step_head(s), it = step_tile(s);
-            const int q = it * 128 + wq * 32 + lane;
-            float* row = p.dQ + (static_cast<size_t>(bh) * N + (q < N ? q : 0)) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
@@ -336,12 +337,26 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     tc_fence_before();
                     mbar_arrive(&bar_dq_free);
                 }
-                if (q < N) {
+                if (lane == 0) bulk_wait_group_read<0>();  // the staging buffer's previous box was read
+                __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) atomicAdd(row + c * 32 + i, __uint_as_float(v[i]) * p.scale);
+                for (int k = 0; k < 8; ++k)
+                    st_shared_v4(stage + lane * 128 + ((k ^ (lane & 7)) << 4),
+                                 __float_as_uint(__uint_as_float(v[4 * k]) * p.scale),
+                                 __float_as_uint(__uint_as_float(v[4 * k + 1]) * p.scale),
+                                 __float_as_uint(__uint_as_float(v[4 * k + 2]) * p.scale),
+                                 __float_as_uint(__uint_as_float(v[4 * k + 3]) * p.scale));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {  // rows past N are not written by the reduction
+                    tma_reduce_add_3d(&tmDQ, smem + C::OFF_DQS + wq * 4096, c * 32, it * 128 + wq * 32, bh);
+                    bulk_commit_group();
                 }
+                __syncwarp();
             }
         }
+        if (lane == 0) bulk_wait_group_all();  // every reduction of this warp performed
+        __syncwarp();
     }
 
     tc_fence_before();

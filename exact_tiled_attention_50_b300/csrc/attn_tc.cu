@@ -603,6 +603,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             bv[c] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
+                    // the row's bias two tiles ahead (one tile ahead as well at the first step) into L2,
+                    // so that the loads above find it there; only 128-byte lines inside the row's N keys
+                    if (brow != nullptr) {
+#pragma unroll
+                        for (int a = (jj == 0 ? 1 : 2); a <= 2; ++a) {
+                            const int kp = kb + a * BLOCK_N;
+                            if (jj + a < nkvt) {
+                                if (kp + 64 <= p.plan.N) prefetch_l2(brow + kp);
+                                if (kp + 128 <= p.plan.N) prefetch_l2(brow + kp + 64);
+                            }
+                        }
+                    }
                 }
                 // tcgen05.ld/st below are warp-collective: the warp proceeds only if every lane's wait
                 // succeeded

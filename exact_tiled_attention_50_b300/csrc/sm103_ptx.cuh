@@ -136,6 +136,10 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
                  "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
+// Fetch the 128-byte line holding `addr` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* addr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(addr)));
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's bulk groups still read their shared-memory source.
 template <int N>
