@@ -10,10 +10,13 @@
 // shared memory and accumulates dK_j and dV_j in tensor memory over every query head of its group and
 // every query tile (causal: the tiles at or after the key tile). Per query tile:
 //   MMA warp      S^T = K_j Q_i^T, dP^T = V_j dO_i^T         (TMEM cols 0-127, 128-255)
-//   warps 0-3     one key row each: P^T, dS^T -> bf16 in shared memory (128-byte swizzled)
-//   MMA warp      dV += P^T dO_i, dK += dS^T Q_i, dQ_i = dS K_j   (dQ in cols 0-127)
-//   warps 4-7     one query row each: dQ_i scaled, staged in shared memory and added into the fp32 dQ
-//                 in device memory by bulk tensor reductions (several key tiles add into the same rows)
+//   warps 0-7     one key row each (warps 0-3 queries 0-63, warps 4-7 queries 64-127): P^T, dS^T ->
+//                 bf16 in shared memory (128-byte swizzled)
+//   MMA warp      dV += P^T dO_i, dK += dS^T Q_i (then Q_i, dO_i are released to the next loads),
+//                 dQ_i = dS K_j   (dQ in cols 0-127)
+//   warps 4-7     then one query row each: dQ_i scaled, staged in shared memory and added into the
+//                 fp32 dQ in device memory by bulk tensor reductions (several key tiles add into the
+//                 same rows); warps 0-3 write dK_j, dV_j at the end
 //   warp 9        TMA loads (K_j, V_j once; Q_i, dO_i and the row statistics per tile)
 // All waits are bounded as in the forward kernel; a wait that runs out records an error bit.
 #include <cuda.h>
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         mbar_init(&bar_qdo_full, 1);
         mbar_init(&bar_qdo_empty, 1);
         mbar_init(&bar_s_full, 1);
-        mbar_init(&bar_ps_full, 128);
+        mbar_init(&bar_ps_full, 256);
         mbar_init(&bar_ps_empty, 1);
         mbar_init(&bar_dq_full, 1);
         mbar_init(&bar_dq_free, 128);
@@ -198,12 +201,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     umma_ss(tmem + C::T_DK, dDST_k + kmaj(kk), dQ_mn + mnmaj(kk), C::IDESC_KV, (s > 0 || kk > 0));
+                umma_commit(&bar_qdo_empty);  // Q_i, dO_i read: the next tile's loads overlap the dQ product
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // contraction over the 128 keys
                     umma_ss(tmem + C::T_DQ, dDS_mn + mnmaj(kk), dK_mn + mnmaj(kk), C::IDESC_Q, kk > 0);
                 umma_commit(&bar_dq_full);
                 umma_commit(&bar_ps_empty);
-                umma_commit(&bar_qdo_empty);
             }
             __syncwarp();
         }
@@ -212,9 +215,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         volatile int never = 0;
         const bool drained = mbar_wait(&bar_done, 0, limit_ns, &never);
         if (!__all_sync(0xffffffffu, drained) && lane == 0) bw_fail(&abort_flag, ERRBIT_WAIT_DRAIN);
-    } else if (warp < 4) {
-        // ============== warps 0-3: one key row each; P^T and dS^T into shared memory ==============
-        const int r = warp * 32 + lane;          // key row in the tile
+    } else if (warp < 8) {
+        // ==== warps 0-7: one key row each, warps 0-3 for queries 0-63 and warps 4-7 for queries 64-127;
+        // P^T and dS^T into shared memory. Warps 4-7 then read dQ_i out of tensor memory as well. ====
+        const int half = warp >> 2;
+        const int r = (warp & 3) * 32 + lane;    // key row in the tile
         const int key = k0 + r;
         const uint32_t lane_off = tmem_lane_base(warp);
         const float sl = p.scale_log2;
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             }
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {        // 32 queries at a time
+            for (int c = 2 * half; c < 2 * half + 2; ++c) {  // 32 queries at a time
                 uint32_t sv[32], dpv[32];
                 tmem_ld32(tmem + lane_off + C::T_S + c * 32, sv);
                 tmem_ld32(tmem + lane_off + C::T_DP + c * 32, dpv);
@@ -272,9 +277,53 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             fence_proxy_async_smem();  // the MMAs read P^T and dS^T through the async proxy
             tc_fence_before();
             mbar_arrive(&bar_ps_full);
+            if (half == 1) {
+                // dQ_i (query rows 32 (warp - 4) ..): scaled, staged in shared memory and added into device
+                // memory by bulk tensor reductions (several key tiles add into the same dQ rows)
+                const bool gq = mbar_wait(&bar_dq_full, s & 1, limit_ns, &abort_flag);
+                if (!__all_sync(0xffffffffu, gq)) {
+                    if (!gq) bw_fail(&abort_flag, ERRBIT_WAIT_O);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int bh = b * p.H + step_head(s);
+                const int wq = warp & 3;
+                const uint32_t stage = smem_u32(smem + C::OFF_DQS + wq * 4096);
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + C::T_DQ + c * 32, v);
+                    tmem_wait_ld(v);
+                    if (c == D / 32 - 1) {  // tensor memory read out: the next S^T may overwrite it
+                        tc_fence_before();
+                        mbar_arrive(&bar_dq_free);
+                    }
+                    if (lane == 0) bulk_wait_group_read<0>();  // the staging buffer's previous box was read
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        st_shared_v4(stage + lane * 128 + ((k ^ (lane & 7)) << 4),
+                                     __float_as_uint(__uint_as_float(v[4 * k]) * p.scale),
+                                     __float_as_uint(__uint_as_float(v[4 * k + 1]) * p.scale),
+                                     __float_as_uint(__uint_as_float(v[4 * k + 2]) * p.scale),
+                                     __float_as_uint(__uint_as_float(v[4 * k + 3]) * p.scale));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {  // rows past N are not written by the reduction
+                        tma_reduce_add_3d(&tmDQ, smem + C::OFF_DQS + wq * 4096, c * 32, it * 128 + wq * 32, bh);
+                        bulk_commit_group();
+                    }
+                    __syncwarp();
+                }
+            }
         }
-        // ---- dK, dV of this key tile: fp32 rows straight to device memory ----
-        if (ok && n_steps > 0) {
+        if (half == 1) {
+            if (lane == 0) bulk_wait_group_all();  // every reduction of this warp performed
+            __syncwarp();
+        }
+        // ---- dK, dV of this key tile (warps 0-3): fp32 rows straight to device memory ----
+        if (half == 0 && ok && n_steps > 0) {
             const bool got = mbar_wait(&bar_done, 0, limit_ns, &abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
                 if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_DRAIN);
@@ -284,7 +333,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         }
         // ok and n_steps are warp-uniform; key < N is not (the last key tile of a ragged N), so every
         // lane takes part in the warp-collective tensor-memory loads and only the stores are guarded.
-        if (ok) {
+        if (half == 0 && ok) {
             const bool row_ok = key < N;
             const size_t orow = (static_cast<size_t>(zkv) * N + (row_ok ? key : 0)) * D;
 #pragma unroll 1
@@ -311,52 +360,6 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 }
             }
         }
-    } else if (warp < 8) {
-        // ===== warps 4-7: one query row each; dQ_i scaled and added into device memory by the tensor =====
-        // store engine (bulk reduce-add of 32 x 32 fp32 boxes staged in shared memory; several key
-        // tiles add into the same dQ rows, the reductions happen at L2)
-        const int wq = warp & 3;
-        const uint32_t lane_off = tmem_lane_base(wq);
-        const uint32_t stage = smem_u32(smem + C::OFF_DQS + wq * 4096);
-        bool ok = true;
-        for (int s = 0; s < n_steps && ok; ++s) {
-            const bool got = mbar_wait(&bar_dq_full, s & 1, limit_ns, &abort_flag);
-            if (!__all_sync(0xffffffffu, got)) {
-                if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_O);
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const int bh = b * p.H + step_head(s), it = step_tile(s);
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + C::T_DQ + c * 32, v);
-                tmem_wait_ld(v);
-                if (c == D / 32 - 1) {  // tensor memory read out: the next S^T may overwrite it
-                    tc_fence_before();
-                    mbar_arrive(&bar_dq_free);
-                }
-                if (lane == 0) bulk_wait_group_read<0>();  // the staging buffer's previous box was read
-                __syncwarp();
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    st_shared_v4(stage + lane * 128 + ((k ^ (lane & 7)) << 4),
-                                 __float_as_uint(__uint_as_float(v[4 * k]) * p.scale),
-                                 __float_as_uint(__uint_as_float(v[4 * k + 1]) * p.scale),
-                                 __float_as_uint(__uint_as_float(v[4 * k + 2]) * p.scale),
-                                 __float_as_uint(__uint_as_float(v[4 * k + 3]) * p.scale));
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {  // rows past N are not written by the reduction
-                    tma_reduce_add_3d(&tmDQ, smem + C::OFF_DQS + wq * 4096, c * 32, it * 128 + wq * 32, bh);
-                    bulk_commit_group();
-                }
-                __syncwarp();
-            }
-        }
-        if (lane == 0) bulk_wait_group_all();  // every reduction of this warp performed
-        __syncwarp();
     }
 
     tc_fence_before();
