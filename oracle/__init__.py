@@ -135,5 +135,6 @@ def attention_tiled(q, k, v, scale, causal=False, kv_len=None, Br=16, Bc=16):
     return O, LSE
 
 
-from .attn_oracle_np import (attention_bwd_np, attention_fp8_np, attention_np, e4m3_round, fwht_f32,  # noqa: E402
-                             merge_np, quantize_e4m3_tiles, tile_exponent)
+from .attn_oracle_np import (attention_bias_dropout_np, attention_bwd_np, attention_fp8_np,  # noqa: E402
+                             attention_np, dropout_keep_mask, dropout_threshold, e4m3_round, fwht_f32, merge_np,
+                             philox4x32_10, quantize_e4m3_tiles, tile_exponent)
