@@ -59,6 +59,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of `values` over every rank of the default process group (the slowest
+    rank sets a job's time); the values themselves when there is no process group."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_value(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time (ms), in
+    units per second divided by 1e12 (TFLOP/s for FLOP units)."""
+    return world * units_per_rank / (ms * 1e-3) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
 
@@ -275,10 +292,7 @@ def run_ours(args, w):
         raise RuntimeError(f"timed run failed: {attn.status_string(rc)}")
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     kern_ms = sum(attn.event_elapsed_ms(a, b) for a, b in kev) / K
-    if ws > 1:
-        t = torch.tensor([step_ms, kern_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, kern_ms = float(t[0]), float(t[1])
+    step_ms, kern_ms = max_over_ranks([step_ms, kern_ms], device=dev)
 
     # ---- end to end through the public API: pinned host inputs -> device -> attn_fwd -> host ----
     hq, hk, hv = x.q.pin_memory(), x.k.pin_memory(), x.v.pin_memory()
@@ -305,10 +319,7 @@ def run_ours(args, w):
         if i > 0:
             e2e_ms.append(e0.elapsed_time(e1))
     e2e = sum(e2e_ms) / len(e2e_ms)
-    if ws > 1:
-        t = torch.tensor([e2e], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e = float(t[0])
+    (e2e,) = max_over_ranks([e2e], device=dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv)) + (hkv.numel() * 4 if hkv is not None else 0)
     d2h = ho.numel() * 4 + hl.numel() * 4
 
@@ -328,7 +339,7 @@ def run_ours(args, w):
                 "algorithmic_bytes": nbytes, "tensor_tflops": achieved}
     line = {
         "metric": {"fp8": METRIC_FP8, "bias_dropout": METRIC_EX, "dropout": METRIC_EX}.get(args.path, METRIC),
-        "value": ws * flops / (step_ms * 1e-3) / 1e12,
+        "value": job_value(flops, ws, step_ms),
         "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1), 1% of key rows x8)",
@@ -350,7 +361,7 @@ def run_ours(args, w):
                                      if fp8 else f"{peaks['source']} " + ("copy bandwidth" if bias is not None
                                                                           else "bf16 burst (cuBLAS)"))
                                     + f"; tensor frac of sustained {achieved / peak_sus:.3f}"},
-        "e2e": {"value": ws * flops / (e2e * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_value(flops, ws, e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
         "gpu_launches": K * attn.launches_per_call(q.dtype),
         "clocks": clocks,
