@@ -102,10 +102,11 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // 3-D map over [slabs, rows, d] 16-bit values: box of 64 columns x 128 rows, 128-byte swizzle,
 // rows past `rows` in a slab read as zero.
-bool encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int d, int rows, long long slabs) {
+bool encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int d, int rows, long long slabs,
+                     unsigned box_rows) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(slabs)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -115,10 +116,10 @@ bool encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, i
 
 // 3-D map over the fp32 output [slabs, rows, d]: box of 32 columns x 32 rows, 128-byte swizzle
 // (the layout the epilogue stages rows in); rows past `rows` are not written by stores.
-bool encode_out_map(CUtensorMap* m, void* base, int d, int rows, long long slabs) {
+bool encode_out_map(CUtensorMap* m, void* base, int d, int rows, long long slabs, unsigned box_rows) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(slabs)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(rows) * d * 4};
-    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t box[3] = {32, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -159,10 +160,13 @@ MapEntry g_map_cache[kMapCache];
 int g_map_next = 0;
 std::mutex g_map_mutex;
 
-enum { MAP_Q_BF16 = 0, MAP_K_BF16 = 1, MAP_V_F16 = 2, MAP_O_F32 = 3, MAP_U8 = 4 };
+// MAP_Q64_BF16: bf16 rows in boxes of 64 columns x 64 rows; MAP_O64_F32: fp32 boxes of 32 x 64 (the
+// d = 128 backward's query tiles and dQ reductions); the others as described above.
+enum { MAP_Q_BF16 = 0, MAP_K_BF16 = 1, MAP_V_F16 = 2, MAP_O_F32 = 3, MAP_U8 = 4, MAP_Q64_BF16 = 5, MAP_O64_F32 = 6 };
 
-bool encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int d, int rows, long long slabs);
-bool encode_out_map(CUtensorMap* m, void* base, int d, int rows, long long slabs);
+bool encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int d, int rows, long long slabs,
+                     unsigned box_rows);
+bool encode_out_map(CUtensorMap* m, void* base, int d, int rows, long long slabs, unsigned box_rows);
 bool encode_u8_map(CUtensorMap* m, const void* base, int inner, int rows, long long slabs);
 
 bool get_map(CUtensorMap* m, int kind, const void* base, int d, int rows, long long slabs) {
@@ -176,10 +180,11 @@ bool get_map(CUtensorMap* m, int kind, const void* base, int d, int rows, long l
             }
     }
     bool ok = false;
-    if (kind == MAP_O_F32) ok = encode_out_map(m, const_cast<void*>(base), d, rows, slabs);
+    if (kind == MAP_O_F32 || kind == MAP_O64_F32)
+        ok = encode_out_map(m, const_cast<void*>(base), d, rows, slabs, kind == MAP_O64_F32 ? 64 : 32);
     else if (kind == MAP_U8) ok = encode_u8_map(m, base, d, rows, slabs);
     else ok = encode_rows_map(m, base, kind == MAP_V_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                              d, rows, slabs);
+                              d, rows, slabs, kind == MAP_Q64_BF16 ? 64 : 128);
     if (!ok) return false;
     std::lock_guard<std::mutex> lock(g_map_mutex);
     MapEntry& e = g_map_cache[g_map_next];
@@ -476,11 +481,13 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const float* O
     float* dvec = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + half);
 
     CUtensorMap tmQ, tmK, tmV, tmDO, tmDQ;
-    if (!get_map(&tmQ, MAP_Q_BF16, Q, d, N, static_cast<long long>(B) * H) ||
+    // d = 128 runs the kernel with 64-row query tiles (its Q, dO and dQ maps have 64-row boxes)
+    const bool q64 = d == 128;
+    if (!get_map(&tmQ, q64 ? MAP_Q64_BF16 : MAP_Q_BF16, Q, d, N, static_cast<long long>(B) * H) ||
         !get_map(&tmK, MAP_K_BF16, K, d, N, static_cast<long long>(B) * H_kv) ||
         !get_map(&tmV, MAP_K_BF16, V, d, N, static_cast<long long>(B) * H_kv) ||
-        !get_map(&tmDO, MAP_Q_BF16, dO, d, N, static_cast<long long>(B) * H) ||
-        !get_map(&tmDQ, MAP_O_F32, dQ, d, N, static_cast<long long>(B) * H))
+        !get_map(&tmDO, q64 ? MAP_Q64_BF16 : MAP_Q_BF16, dO, d, N, static_cast<long long>(B) * H) ||
+        !get_map(&tmDQ, q64 ? MAP_O64_F32 : MAP_O_F32, dQ, d, N, static_cast<long long>(B) * H))
         return ATTN_ERR_UNSUPPORTED;
 
     attn_impl::BwdPrepParams pp{};

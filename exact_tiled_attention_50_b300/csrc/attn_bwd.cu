@@ -61,6 +61,10 @@ struct BwCfg {
     static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 384, T_DQ = 0;
 };
 
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ void bw_fail(volatile int* abort_flag, uint32_t bits) {
     *abort_flag = 1;
     atomicOr(&g_attn_bwd_error, ERRBIT_TIMEOUT | bits);
@@ -370,6 +374,360 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// d = 128: query tiles of 64 rows through a two-stage Q/dO ring, so that the next tile's loads and
+// its S^T, dP^T products overlap the current tile's P/dS work and dV, dK, dQ products. Per step s
+// (query tile i of one head of the group) the MMA warp issues S^T(s), dP^T(s) (M = 128 keys, N = 64
+// queries), then the second-phase products of step s - 1: dV += P^T dO, dK += dS^T Q (which release
+// the ring stage), dQ^T = K^T dS^T (M = d, N = 64 queries) into one of two TMEM buffers. Warps 0-7
+// compute P^T, dS^T (one key row per thread, 32 queries each); warps 0-3 then read dQ^T of the
+// previous step (one dimension per thread), stage it as [64 queries][32 dims] and reduce it into dQ.
+// ---------------------------------------------------------------------------------------------
+struct Bw2Cfg {
+    static constexpr int D = 128;
+    static constexpr int QT = 64;                        // query rows per step
+    static constexpr int OFF_K = 0, OFF_V = 32768;       // 128 keys x 128 dims bf16, two 64-column boxes
+    static constexpr int OFF_RING = 65536;
+    static constexpr int QD = 16384;                     // 64 rows x 128 dims bf16: two boxes of 8 KB
+    static constexpr int STAGE = 2 * QD + 1024;          // Q, dO, then lse2[64], dvec[64]
+    static constexpr int OFF_PT = OFF_RING + 2 * STAGE;  // P^T [128 keys][64 queries] bf16 (128 B rows)
+    static constexpr int OFF_DST = OFF_PT + 16384;       // dS^T, same layout
+    static constexpr int OFF_DQS = OFF_DST + 16384;      // 4 warps x [64 queries][32 dims] fp32, swizzled
+    static constexpr int SMEM = 1024 + OFF_DQS + 4 * 8192;
+    static constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 256, T_DK = 384;  // dQ^T: 2 x 64 columns
+    static constexpr uint32_t IDESC_SD = idesc_f16(128, 64, 1, 1, 0, 0);   // S^T, dP^T: K-major A and B
+    static constexpr uint32_t IDESC_KV = idesc_f16(128, 128, 1, 1, 0, 1);  // dV, dK: A K-major, B MN-major
+    static constexpr uint32_t IDESC_Q = idesc_f16(128, 64, 1, 1, 1, 1);    // dQ^T: A (K^T), B (dS^T) MN-major
+};
+static_assert(Bw2Cfg::SMEM <= 232448, "shared memory");
+static_assert(Bw2Cfg::OFF_PT % 1024 == 0 && Bw2Cfg::OFF_DQS % 1024 == 0 && Bw2Cfg::STAGE % 1024 == 0, "align");
+
+__global__ void __launch_bounds__(BW_THREADS, 1)
+    attn_bwd_q64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                        const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdParams p) {
+    using C = Bw2Cfg;
+    constexpr int D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bar_kv, bar_qdo_full[2], bar_qdo_empty[2], bar_s_full, bar_sdp_free,
+        bar_ps_full, bar_ps_empty, bar_dq_full[2], bar_dq_free[2], bar_done;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int jt = blockIdx.x;                 // key tile (128 keys)
+    const int zkv = blockIdx.y;                // b * H_kv + kv head
+    const int b = zkv / p.H_kv, hk = zkv - b * p.H_kv;
+    const int N = p.N;
+    int kv_valid = N;
+    if (p.kv_len) {
+        kv_valid = __ldg(p.kv_len + b);
+        kv_valid = kv_valid < 0 ? 0 : (kv_valid > N ? N : kv_valid);
+    }
+    const int k0 = jt * 128;
+    const bool any_keys = k0 < kv_valid;
+    const int n_q64 = (N + C::QT - 1) / C::QT;
+    const int i_first = p.causal ? 2 * jt : 0;  // 64-row query tiles with at least one valid pair
+    const int n_i = any_keys ? n_q64 - i_first : 0;
+    const int n_steps = n_i * p.group;
+    const uint64_t limit_ns = p.wait_limit_ns;
+
+    if (warp == BW_MMA_WARP) {
+        tmem_alloc(&tmem_base_sh, 512);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(&bar_kv, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_qdo_full[i], 1);
+            mbar_init(&bar_qdo_empty[i], 1);
+            mbar_init(&bar_dq_full[i], 1);
+            mbar_init(&bar_dq_free[i], 128);
+        }
+        mbar_init(&bar_s_full, 1);
+        mbar_init(&bar_sdp_free, 256);
+        mbar_init(&bar_ps_full, 256);
+        mbar_init(&bar_ps_empty, 1);
+        mbar_init(&bar_done, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    auto step_head = [&](int s) { return hk * p.group + s / n_i; };
+    auto step_tile = [&](int s) { return i_first + s % n_i; };
+    auto stage_ptr = [&](int s) { return smem + C::OFF_RING + (s & 1) * C::STAGE; };
+
+    if (warp == BW_TMA_WARP) {
+        // ================================ TMA producer (one lane) ================================
+        if (elect_one() && n_steps > 0) {
+            mbar_arrive_expect_tx(&bar_kv, 2 * 32768);
+            for (int bx = 0; bx < 2; ++bx) {
+                tma_load_3d(smem + C::OFF_K + bx * 16384, &tmK, &bar_kv, bx * 64, k0, zkv);
+                tma_load_3d(smem + C::OFF_V + bx * 16384, &tmV, &bar_kv, bx * 64, k0, zkv);
+            }
+            int issued = 0;
+            for (int s = 0; s < n_steps; ++s) {
+                const int st = s & 1;
+                if (s >= 2 && !mbar_wait(&bar_qdo_empty[st], ((s >> 1) - 1) & 1, limit_ns, &abort_flag)) {
+                    bw_fail(&abort_flag, ERRBIT_WAIT_EMPTY);
+                    break;
+                }
+                const int bh = b * p.H + step_head(s), it = step_tile(s);
+                uint8_t* sp = stage_ptr(s);
+                mbar_arrive_expect_tx(&bar_qdo_full[st], 2 * C::QD + 512);
+                for (int bx = 0; bx < 2; ++bx) {
+                    tma_load_3d(sp + bx * 8192, &tmQ, &bar_qdo_full[st], bx * 64, it * C::QT, bh);
+                    tma_load_3d(sp + C::QD + bx * 8192, &tmDO, &bar_qdo_full[st], bx * 64, it * C::QT, bh);
+                }
+                const size_t srow = static_cast<size_t>(bh) * p.n_qt * 128 + static_cast<size_t>(it) * C::QT;
+                bulk_load(sp + 2 * C::QD, p.lse2 + srow, 256, &bar_qdo_full[st]);
+                bulk_load(sp + 2 * C::QD + 256, p.dvec + srow, 256, &bar_qdo_full[st]);
+                issued = s + 1;
+            }
+            if (abort_flag) {  // wait (bounded) for the copies in flight before the CTA may exit
+                volatile int never = 0;
+                (void)mbar_wait(&bar_kv, 0, limit_ns, &never);
+                for (int s = issued > 2 ? issued - 2 : 0; s < issued; ++s)
+                    (void)mbar_wait(&bar_qdo_full[s & 1], (s >> 1) & 1, limit_ns, &never);
+            }
+        }
+        __syncwarp();
+    } else if (warp == BW_MMA_WARP) {
+        // ======================================= MMA issuer =======================================
+        auto wait_all = [&](uint64_t* bar, uint32_t parity, uint32_t bit) {
+            const bool got = mbar_wait(bar, parity, limit_ns, &abort_flag);
+            if (__all_sync(0xffffffffu, got)) return true;
+            if (!got) bw_fail(&abort_flag, bit);
+            return false;
+        };
+        const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);      // K as K-major A
+        const uint64_t dV_k = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);      // V as K-major A
+        const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + C::OFF_K), 16384, 1024);  // K^T as M-major A
+        const uint64_t dPT_k = sdesc_sw128(smem_u32(smem + C::OFF_PT), 16, 1024);    // P^T as K-major A
+        const uint64_t dDST_k = sdesc_sw128(smem_u32(smem + C::OFF_DST), 16, 1024);  // dS^T as K-major A
+        const uint64_t dDST_n = sdesc_sw128(smem_u32(smem + C::OFF_DST), 16384, 1024);  // dS^T as N-major B
+        // K and V tiles: k-step kk of 16 dims (two 16 KB boxes of 64 dims); Q, dO tiles: 8 KB boxes
+        auto kmaj_kv = [](int kk) { return static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
+        auto kmaj_q = [](int kk) { return static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4); };
+        auto rows16 = [](int kk) { return static_cast<uint64_t>((kk * 2048) >> 4); };  // 16 rows of 128 B
+        auto col16 = [](int kk) { return static_cast<uint64_t>((kk * 32) >> 4); };      // 16 elements of a row
+        bool ok = n_steps > 0 ? wait_all(&bar_kv, 0, ERRBIT_WAIT_KV) : true;
+        for (int s = 0; s <= n_steps && ok; ++s) {
+            if (s < n_steps) {
+                // ---- S^T(s) = K Q^T, dP^T(s) = V dO^T ----
+                if (!wait_all(&bar_qdo_full[s & 1], (s >> 1) & 1, ERRBIT_WAIT_Q)) { ok = false; break; }
+                if (s > 0 && !wait_all(&bar_sdp_free, (s - 1) & 1, ERRBIT_WAIT_P)) { ok = false; break; }
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint32_t sp = smem_u32(stage_ptr(s));
+                    const uint64_t dQ_k = sdesc_sw128(sp, 16, 1024);
+                    const uint64_t dDO_k = sdesc_sw128(sp + C::QD, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_ss(tmem + C::T_S, dK_k + kmaj_kv(kk), dQ_k + kmaj_q(kk), C::IDESC_SD, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_ss(tmem + C::T_DP, dV_k + kmaj_kv(kk), dDO_k + kmaj_q(kk), C::IDESC_SD, kk > 0);
+                    umma_commit(&bar_s_full);
+                }
+                __syncwarp();
+            }
+            if (s >= 1) {
+                // ---- second phase of step t = s - 1 ----
+                const int t = s - 1;
+                if (!wait_all(&bar_ps_full, t & 1, ERRBIT_WAIT_P)) { ok = false; break; }
+                if (t >= 2 && !wait_all(&bar_dq_free[t & 1], ((t >> 1) - 1) & 1, ERRBIT_WAIT_O)) { ok = false; break; }
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint32_t sp = smem_u32(stage_ptr(t));
+                    const uint64_t dQ_mn = sdesc_sw128(sp, 8192, 1024);            // Q as MN-major B (N = dims)
+                    const uint64_t dDO_mn = sdesc_sw128(sp + C::QD, 8192, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < C::QT / 16; ++kk)  // contraction over the 64 queries
+                        umma_ss(tmem + C::T_DV, dPT_k + col16(kk), dDO_mn + rows16(kk), C::IDESC_KV, (t > 0 || kk > 0));
+#pragma unroll
+                    for (int kk = 0; kk < C::QT / 16; ++kk)
+                        umma_ss(tmem + C::T_DK, dDST_k + col16(kk), dQ_mn + rows16(kk), C::IDESC_KV, (t > 0 || kk > 0));
+                    umma_commit(&bar_qdo_empty[t & 1]);  // Q, dO of step t read: the stage may be refilled
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T: contraction over the 128 keys
+                        umma_ss(tmem + C::T_DQ + 64 * (t & 1), dK_mn + rows16(kk), dDST_n + rows16(kk), C::IDESC_Q, kk > 0);
+                    umma_commit(&bar_dq_full[t & 1]);
+                    umma_commit(&bar_ps_empty);
+                }
+                __syncwarp();
+            }
+        }
+        if (elect_one()) umma_commit(&bar_done);  // every MMA issued above has completed
+        __syncwarp();
+        volatile int never = 0;
+        const bool drained = mbar_wait(&bar_done, 0, limit_ns, &never);
+        if (!__all_sync(0xffffffffu, drained) && lane == 0) bw_fail(&abort_flag, ERRBIT_WAIT_DRAIN);
+    } else if (warp < 8) {
+        // ===== warps 0-7: one key row each, 32 queries (warps 0-3: queries 0-31, warps 4-7: 32-63) =====
+        const int qh = warp >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;            // key row in the tile
+        const int key = k0 + r;
+        const uint32_t lane_off = tmem_lane_base(warp);
+        const float sl = p.scale_log2;
+        const uint32_t pt_row = smem_u32(smem + C::OFF_PT) + r * 128;
+        const uint32_t dst_row = smem_u32(smem + C::OFF_DST) + r * 128;
+        const uint32_t stage = smem_u32(smem + C::OFF_DQS + wq * 8192);
+        bool ok = true;
+        // dQ of step t (warps 0-3): dQ^T from tensor memory (this thread: dimension 32 wq + lane, 64
+        // queries), staged as [64 queries][32 dims] (128-byte swizzled) and reduced into dQ
+        auto dq_out = [&](int t) -> bool {
+            const bool got = mbar_wait(&bar_dq_full[t & 1], (t >> 1) & 1, limit_ns, &abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_O);
+                return false;
+            }
+            tc_fence_after();
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tmem + lane_off + C::T_DQ + 64 * (t & 1), v0);
+            tmem_ld32(tmem + lane_off + C::T_DQ + 64 * (t & 1) + 32, v1);
+            tmem_wait_ld(v0);
+            tmem_wait_ld(v1);
+            tc_fence_before();
+            mbar_arrive(&bar_dq_free[t & 1]);
+            if (lane == 0) bulk_wait_group_read<0>();  // the staging buffer's previous box was read
+            __syncwarp();
+            const uint32_t colb = (lane & 3) * 4;
+#pragma unroll
+            for (int q = 0; q < 64; ++q) {
+                const float val = __uint_as_float(q < 32 ? v0[q] : v1[q - 32]) * p.scale;
+                st_shared_f32(stage + q * 128 + ((((lane >> 2) ^ (q & 7))) << 4) + colb, val);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {  // rows past N are not written by the reduction
+                const int bh = b * p.H + step_head(t), it = step_tile(t);
+                tma_reduce_add_3d(&tmDQ, smem + C::OFF_DQS + wq * 8192, wq * 32, it * C::QT, bh);
+                bulk_commit_group();
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int s = 0; s < n_steps && ok; ++s) {
+            const int it = step_tile(s);
+            const int q0 = it * C::QT + 32 * qh;
+            const float* lse2 = reinterpret_cast<const float*>(stage_ptr(s) + 2 * C::QD) + 32 * qh;
+            const float* dvec = lse2 + 64;
+            bool got = mbar_wait(&bar_s_full, s & 1, limit_ns, &abort_flag);
+            got = got && mbar_wait(&bar_qdo_full[s & 1], (s >> 1) & 1, limit_ns, &abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_S);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[32], dpv[32];
+            tmem_ld32(tmem + lane_off + C::T_S + 32 * qh, sv);
+            tmem_ld32(tmem + lane_off + C::T_DP + 32 * qh, dpv);
+            tmem_wait_ld(sv);
+            tmem_wait_ld(dpv);
+            tc_fence_before();
+            mbar_arrive(&bar_sdp_free);  // S^T, dP^T of this step are in registers: the next may land
+            uint32_t pp[16], dd[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                float pv[2], dv[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int q = q0 + i + u;
+                    const bool valid = key < kv_valid && q < N && (!p.causal || key <= q);
+                    const float e = valid ? ex2_approx(__uint_as_float(sv[i + u]) * sl - lse2[i + u]) : 0.f;
+                    pv[u] = e;
+                    dv[u] = e * (__uint_as_float(dpv[i + u]) - dvec[i + u]);
+                }
+                __nv_bfloat162 ph = __floats2bfloat162_rn(pv[0], pv[1]);
+                __nv_bfloat162 dh = __floats2bfloat162_rn(dv[0], dv[1]);
+                pp[i / 2] = *reinterpret_cast<uint32_t*>(&ph);
+                dd[i / 2] = *reinterpret_cast<uint32_t*>(&dh);
+            }
+            // P^T, dS^T of the previous step must have been consumed by its products
+            if (s > 0) {
+                const bool e = mbar_wait(&bar_ps_empty, (s - 1) & 1, limit_ns, &abort_flag);
+                if (!__all_sync(0xffffffffu, e)) {
+                    if (!e) bw_fail(&abort_flag, ERRBIT_WAIT_EMPTY);
+                    ok = false;
+                    break;
+                }
+            }
+            // 32 queries = four 16-byte chunks (4 qh .. 4 qh + 3) of this key's 128-byte row
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t off = ((4 * qh + k) ^ (r & 7)) << 4;
+                st_shared_v4(pt_row + off, pp[4 * k], pp[4 * k + 1], pp[4 * k + 2], pp[4 * k + 3]);
+                st_shared_v4(dst_row + off, dd[4 * k], dd[4 * k + 1], dd[4 * k + 2], dd[4 * k + 3]);
+            }
+            fence_proxy_async_smem();  // the MMAs read P^T and dS^T through the async proxy
+            tc_fence_before();
+            mbar_arrive(&bar_ps_full);
+            if (qh == 0 && s > 0 && !dq_out(s - 1)) {
+                ok = false;
+                break;
+            }
+        }
+        if (qh == 0) {
+            if (ok && n_steps > 0 && !dq_out(n_steps - 1)) ok = false;
+            if (lane == 0) bulk_wait_group_all();  // every reduction of this warp performed
+            __syncwarp();
+        }
+        // ---- dK, dV of this key tile (warps 0-3): fp32 rows straight to device memory ----
+        if (qh == 0 && ok && n_steps > 0) {
+            const bool got = mbar_wait(&bar_done, 0, limit_ns, &abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_DRAIN);
+                ok = false;
+            }
+            tc_fence_after();
+        }
+        // ok and n_steps are warp-uniform; key < N is not, so every lane takes part in the
+        // warp-collective tensor-memory loads and only the stores are guarded.
+        if (qh == 0 && ok) {
+            const bool row_ok = key < N;
+            const size_t orow = (static_cast<size_t>(zkv) * N + (row_ok ? key : 0)) * D;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                float* dst = (which ? p.dK : p.dV) + orow;
+                const float mul = which ? p.scale : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    if (n_steps > 0) {
+                        tmem_ld32(tmem + lane_off + (which ? C::T_DK : C::T_DV) + c * 32, v);
+                        tmem_wait_ld(v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                    }
+                    if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(dst + c * 32 + i) =
+                                make_float4(__uint_as_float(v[i]) * mul, __uint_as_float(v[i + 1]) * mul,
+                                            __uint_as_float(v[i + 2]) * mul, __uint_as_float(v[i + 3]) * mul);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == BW_MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // D = rowsum(dO * O) and LSE in log2 units for every (padded) query row; dQ rows cleared.
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdPrepParams p) {
     const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // over bh * NQP
@@ -424,7 +782,20 @@ cudaError_t launch_attn_bwd(int d, const BwdPrepParams& prep, const CUtensorMap&
     attn_bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(prep);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (d == 128) return launch_bwd_t<128>(tmQ, tmK, tmV, tmDO, tmDQ, p, stream);
+    if (d == 128) {  // 64-row query tiles through a two-stage ring
+        static std::atomic<int> ready[64];
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64 || ready[dev].load(std::memory_order_acquire) == 0) {
+            e = cudaFuncSetAttribute(attn_bwd_q64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Bw2Cfg::SMEM);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
+        }
+        const dim3 grid(static_cast<unsigned>(p.n_qt), static_cast<unsigned>(p.B * p.H_kv));
+        attn_bwd_q64_kernel<<<grid, BW_THREADS, Bw2Cfg::SMEM, stream>>>(tmQ, tmK, tmV, tmDO, tmDQ, p);
+        return cudaGetLastError();
+    }
     if (d == 64) return launch_bwd_t<64>(tmQ, tmK, tmV, tmDO, tmDQ, p, stream);
     return cudaErrorInvalidValue;
 }

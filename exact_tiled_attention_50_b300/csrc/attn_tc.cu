@@ -1142,8 +1142,8 @@ cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStrea
 // ---------------------------------------------------------------------------------------------
 // fp8 pre-pass (d = 128): one block per 128-row tile of Q, K or V, plus the plan block.
 // Q and K rows are multiplied by the signs and transformed by the unnormalised Walsh-Hadamard
-// butterflies (spans 1, 2 inside a lane, 4 .. 64 across lanes; each output one fp32 addition or
-// subtraction, in that order), then every tile is rounded to E4M3 at its own power-of-two scale.
+// butterflies (spans 1, 2, 4, ..., 64 in that order; each output one fp32 addition or subtraction),
+// then every tile is rounded to E4M3 at its own power-of-two scale.
 // ---------------------------------------------------------------------------------------------
 constexpr int FP8P_THREADS = 256;
 
@@ -1169,60 +1169,66 @@ __device__ __forceinline__ uint32_t fp8_block_max(uint32_t v, uint32_t* red) {
 // 2^-e as fp32 for e in [-100, 120]
 __device__ __forceinline__ float fp8_pow2_neg(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
 
-// One 128-row tile of Q or K: warp w holds rows 16w .. 16w+15, lane l elements 4l .. 4l+3.
+// One 128-row tile of Q or K: thread t holds row t / 2, elements 64 (t mod 2) .. +63. Butterflies
+// of spans 1 .. 32 run inside the thread, span 64 pairs the two threads of a row (lanes 2r, 2r+1).
 __device__ void fp8_prep_qk_tile(const __nv_bfloat16* src, uint8_t* dst, int32_t* exp_out, const int8_t* signs,
                                  int N, int tile, uint32_t* red) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float sg[4] = {1.f, 1.f, 1.f, 1.f};
+    const int half = threadIdx.x & 1;
+    const int row = tile * 128 + (threadIdx.x >> 1);
+    float a[64];
+    if (row < N) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * 128 + half * 64);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint4 u = __ldg(s4 + k);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                a[8 * k + 2 * e] = __uint_as_float(w[e] << 16);
+                a[8 * k + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) a[i] = 0.f;
+    }
     if (signs) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) sg[c] = static_cast<float>(__ldg(signs + 4 * lane + c));
-    }
-    float v[16][4];
-    uint32_t mbits = 0;
+        for (int i = 0; i < 64; ++i) a[i] *= static_cast<float>(__ldg(signs + half * 64 + i));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int row = tile * 128 + warp * 16 + i;
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
-        if (row < N) {
-            const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + static_cast<size_t>(row) * 128) + lane);
-            a[0] = __uint_as_float(u.x << 16);
-            a[1] = __uint_as_float(u.x & 0xffff0000u);
-            a[2] = __uint_as_float(u.y << 16);
-            a[3] = __uint_as_float(u.y & 0xffff0000u);
-        }
-        if (signs) {
+        for (int h = 1; h < 64; h <<= 1) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) a[c] *= sg[c];
-            const float b0 = a[0] + a[1], b1 = a[0] - a[1], b2 = a[2] + a[3], b3 = a[2] - a[3];
-            a[0] = b0 + b2;
-            a[2] = b0 - b2;
-            a[1] = b1 + b3;
-            a[3] = b1 - b3;
-#pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float o = __shfl_xor_sync(0xffffffffu, a[c], m);
-                    a[c] = (lane & m) ? o - a[c] : a[c] + o;
-                }
+            for (int i = 0; i < 64; ++i) {
+                if (i & h) continue;
+                const float x = a[i], y = a[i + h];
+                a[i] = x + y;
+                a[i + h] = x - y;
             }
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            v[i][c] = a[c];
-            mbits = max(mbits, __float_as_uint(a[c]) & 0x7fffffffu);
+        for (int i = 0; i < 64; ++i) {  // span 64: the lower half keeps x + y, the upper x - y
+            const float o = __shfl_xor_sync(0xffffffffu, a[i], 1);
+            a[i] = half ? o - a[i] : a[i] + o;
         }
     }
+    uint32_t mbits = 0;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) mbits = max(mbits, __float_as_uint(a[i]) & 0x7fffffffu);
     const int e = fp8_tile_exponent(fp8_block_max(mbits, red));
     if (threadIdx.x == 0) *exp_out = e;
     const float sc = fp8_pow2_neg(e);
+    if (row < N) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * 128 + half * 64);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int row = tile * 128 + warp * 16 + i;
-        if (row < N)
-            reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(row) * 128)[lane] =
-                pack_e4m3x4(v[i][0] * sc, v[i][1] * sc, v[i][2] * sc, v[i][3] * sc);
+        for (int k = 0; k < 4; ++k) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+                const int i = 16 * k + 4 * e4;
+                w[e4] = pack_e4m3x4(a[i] * sc, a[i + 1] * sc, a[i + 2] * sc, a[i + 3] * sc);
+            }
+            d4[k] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
     }
 }
 
