@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 from exact_tiled_attention_50_b300 import inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s and % of B300 dense-BF16 peak at N=8192, d=128"
+METRIC_BWD = "attention bwd TFLOP/s (10 B H N^2 d) and % of B300 dense-BF16 peak at N=8192, d=128"
 METRIC_EX = "attention fwd TFLOP/s with additive bias and/or dropout p=0.1 at N=8192, d=128"
 METRIC_FP8 = "attention fwd TFLOP/s of the fp8 (E4M3) path and % of B300 dense-FP8 peak at N=8192, d=128"
 UNIT = "TFLOP/s"
@@ -141,10 +142,14 @@ KERNEL_SOURCES = ("exact_tiled_attention_50_b300/csrc/attn_tc.cu", "exact_tiled_
                   "exact_tiled_attention_50_b300/csrc/attn_internal.h")
 
 
-def kernel_source_hash() -> str:
+BWD_SOURCES = ("exact_tiled_attention_50_b300/csrc/attn_bwd.cu", "exact_tiled_attention_50_b300/csrc/sm103_ptx.cuh",
+               "exact_tiled_attention_50_b300/csrc/attn_internal.h")
+
+
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -154,7 +159,9 @@ def profiled_traffic(w, path_kind="bf16"):
     """DRAM bytes per launch of the attention kernel from the committed ncu summary of this workload,
     or None when there is none or the kernel source changed since it was taken."""
     tag = "" if path_kind == "bf16" else "_" + path_kind
-    path = os.path.join(ROOT, "profiles", f"attn_fwd_tc_kernel{tag}_b{w.B}h{w.H}_n{w.N}_d{w.d}.md")
+    name = "attn_bwd_q64_kernel" if path_kind == "bwd" else f"attn_fwd_tc_kernel{tag}"
+    sources = BWD_SOURCES if path_kind == "bwd" else KERNEL_SOURCES
+    path = os.path.join(ROOT, "profiles", f"{name}_b{w.B}h{w.H}_n{w.N}_d{w.d}.md")
     if not os.path.exists(path):
         return None
     kv = {}
@@ -163,7 +170,7 @@ def profiled_traffic(w, path_kind="bf16"):
             m = re.match(r"^(traffic_bytes_per_launch|kernel_source_sha256_16):\s*(\S+)", line)
             if m:
                 kv[m.group(1)] = m.group(2)
-    if kv.get("kernel_source_sha256_16") != kernel_source_hash() or "traffic_bytes_per_launch" not in kv:
+    if kv.get("kernel_source_sha256_16") != kernel_source_hash(sources) or "traffic_bytes_per_launch" not in kv:
         return None
     return float(kv["traffic_bytes_per_launch"])
 
@@ -246,8 +253,17 @@ def run_ours(args, w):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    bwd = args.path == "bwd"
+    if bwd:  # the forward's O and LSE once, and a seeded upstream gradient
+        attn.attn_fwd(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, out=out, lse=lse, workspace=work)
+        gen = torch.Generator().manual_seed(inputs.SEED_BASE + 5000)
+        dO = torch.randn(tuple(q.shape), generator=gen).to(torch.bfloat16).to(dev)
+    grads = []
+
     def step():
-        if fp8:
+        if bwd:
+            grads[:] = attn.attn_bwd(q, k, v, out, dO, lse, scale=x.scale, causal=w.causal, kv_len=kv)
+        elif fp8:
             attn.attn_fwd_fp8(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, signs=signs, out=out, lse=lse,
                               workspace=work)
         elif ex:
@@ -299,6 +315,9 @@ def run_ours(args, w):
     hkv = x.kv_len.pin_memory() if x.kv_len is not None else None
     ho = torch.empty_like(out, device="cpu").pin_memory()
     hl = torch.empty_like(lse, device="cpu").pin_memory()
+    # the backward's extra inputs (dO, and O, LSE of the forward) and its three gradients
+    h_in = [(dO.cpu().pin_memory(), dO), (ho, out), (hl, lse)] if bwd else []
+    h_grads = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in grads] if bwd else []
     e2e_steps = max(1, min(K, args.e2e_steps))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -311,19 +330,27 @@ def run_ours(args, w):
         v.copy_(hv, non_blocking=True)
         if hkv is not None:
             kv.copy_(hkv, non_blocking=True)
+        for h, dvc in h_in:
+            dvc.copy_(h, non_blocking=True)
         step()
-        ho.copy_(out, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+        if bwd:
+            for h, g in zip(h_grads, grads):
+                h.copy_(g, non_blocking=True)
+        else:
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
         if i > 0:
             e2e_ms.append(e0.elapsed_time(e1))
     e2e = sum(e2e_ms) / len(e2e_ms)
     (e2e,) = max_over_ranks([e2e], device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv)) + (hkv.numel() * 4 if hkv is not None else 0)
-    d2h = ho.numel() * 4 + hl.numel() * 4
+    h2d = sum(t.numel() * t.element_size() for t in [hq, hk, hv] + [h for h, _ in h_in]) + \
+        (hkv.numel() * 4 if hkv is not None else 0)
+    d2h = sum(t.numel() * t.element_size() for t in h_grads) if bwd else ho.numel() * 4 + hl.numel() * 4
 
-    flops = flops_of(w)
+    # backward: 5 products of the forward's size (recomputed S, dP, dV, dK, dQ) against its 2
+    flops = flops_of(w) * (2.5 if bwd else 1.0)
     peaks = load_peaks()
     achieved = flops / (kern_ms * 1e-3) / 1e12
     # the contraction's own dtype: E4M3 takes the measured bf16 peak times the nominal fp8 / bf16 ratio
@@ -338,7 +365,8 @@ def run_ours(args, w):
         roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
                 "algorithmic_bytes": nbytes, "tensor_tflops": achieved}
     line = {
-        "metric": {"fp8": METRIC_FP8, "bias_dropout": METRIC_EX, "dropout": METRIC_EX}.get(args.path, METRIC),
+        "metric": {"fp8": METRIC_FP8, "bias_dropout": METRIC_EX, "dropout": METRIC_EX,
+                   "bwd": METRIC_BWD}.get(args.path, METRIC),
         "value": job_value(flops, ws, step_ms),
         "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
@@ -347,7 +375,9 @@ def run_ours(args, w):
                    "in": "bf16", "out": "fp32 O + fp32 LSE",
                    "path": {"fp8": "fp8: Q, K rotated (random signs) + E4M3 per 128-row tile; E4M3 tensor cores",
                             "bias_dropout": "bf16 + additive bf16 bias [B,H,N,N] + dropout p=0.1 (Philox4x32-10)",
-                            "dropout": "bf16 + dropout p=0.1 (Philox4x32-10)"}.get(args.path,
+                            "dropout": "bf16 + dropout p=0.1 (Philox4x32-10)",
+                            "bwd": "backward: dQ, dK, dV (fp32) from bf16 Q, K, V, dO and the forward's O, LSE"
+                            }.get(args.path,
                                                                                   "bf16 tensor cores (fp16 P, fp16 V)"),
                    "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
                    **({"bias": "bf16 [B,H,N,N] resident on the device (not part of the e2e copies)"}
@@ -356,7 +386,9 @@ def run_ours(args, w):
                    "pct_of_peak_bf16": 100.0 * flops / (step_ms * 1e-3) / 1e12 / peaks["bf16"]},
         "roofline": {**roof,
                      "traffic": args.traffic if args.traffic is not None else profiled_traffic(w, args.path),
-                     "kernel": f"attn_fwd_tc_kernel<{w.d},false,{1 if fp8 else 2 if ex else 0}>", "kernel_ms": kern_ms,
+                     "kernel": (("attn_bwd_q64_kernel" if w.d == 128 else f"attn_bwd_tc_kernel<{w.d}>")
+                                + " (with its row-statistics pass)") if bwd
+                     else f"attn_fwd_tc_kernel<{w.d},false,{1 if fp8 else 2 if ex else 0}>", "kernel_ms": kern_ms,
                      "peak_source": (f"{peaks['source']} bf16 burst (cuBLAS) x 2 (nominal fp8/bf16 dense ratio)"
                                      if fp8 else f"{peaks['source']} " + ("copy bandwidth" if bias is not None
                                                                           else "bf16 burst (cuBLAS)"))
@@ -390,7 +422,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--traffic", type=float, default=None, help="DRAM bytes per launch from an ncu capture")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["bf16", "fp8", "bias_dropout", "dropout"], default="bf16",
+    ap.add_argument("--path", choices=["bf16", "fp8", "bias_dropout", "dropout", "bwd"], default="bf16",
                     help="bf16 tensor-core path (the headline) or the fp8 path with incoherent processing")
     args = ap.parse_args()
     if args.warmup < 3:

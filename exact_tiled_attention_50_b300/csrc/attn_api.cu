@@ -499,8 +499,13 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const float* O
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.wait_limit_ns = g_wait_limit_ns.load();
-    return attn_impl::launch_attn_bwd(d, pp, tmQ, tmK, tmV, tmDO, tmDQ, p, stream) == cudaSuccess ? ATTN_OK
-                                                                                                : ATTN_ERR_CUDA;
+    // the timing hook brackets both launches of the backward (its row-statistics pass and the kernel)
+    cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
+    const bool timed = ev0 && ev1;
+    if (timed && cudaEventRecord(ev0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (attn_impl::launch_attn_bwd(d, pp, tmQ, tmK, tmV, tmDO, tmDQ, p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (timed && cudaEventRecord(ev1, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }
 
 attn_status attn_check(cudaStream_t stream) {

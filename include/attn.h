@@ -230,9 +230,10 @@ int attn_debug_schedule(int B, int H, int N, int causal, const int32_t* kv_len_h
                         int max_segments);
 
 /*
- * Timing hook for benchmarks: while set (both non-NULL), every attn_fwd call records `start` on its
- * stream immediately before the main attention kernel and `stop` immediately after it, so that
- * cudaEventElapsedTime gives that kernel's duration on the stream it runs on. The events are
+ * Timing hook for benchmarks: while set (both non-NULL), every attn_fwd, attn_fwd_fp8 and attn_fwd_ex
+ * call records `start` on its stream immediately before the main attention kernel and `stop`
+ * immediately after it (attn_bwd: around its two launches, the row-statistics pass and the kernel),
+ * so that cudaEventElapsedTime gives that duration on the stream the work runs on. The events are
  * created and owned by the caller. attn_set_kernel_events(NULL, NULL) turns the hook off.
  */
 void attn_set_kernel_events(cudaEvent_t start, cudaEvent_t stop);
