@@ -375,13 +375,14 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// d = 128: query tiles of 64 rows through a two-stage Q/dO ring, so that the next tile's loads and
+// d = 128: query tiles of 64 rows through a three-stage Q/dO ring, so that the next tiles' loads and
 // its S^T, dP^T products overlap the current tile's P/dS work and dV, dK, dQ products. Per step s
 // (query tile i of one head of the group) the MMA warp issues S^T(s), dP^T(s) (M = 128 keys, N = 64
 // queries), then the second-phase products of step s - 1: dV += P^T dO, dK += dS^T Q (which release
 // the ring stage), dQ^T = K^T dS^T (M = d, N = 64 queries) into one of two TMEM buffers. Warps 0-7
 // compute P^T, dS^T (one key row per thread, 32 queries each); warps 0-3 then read dQ^T of the
-// previous step (one dimension per thread), stage it as [64 queries][32 dims] and reduce it into dQ.
+// previous step (one dimension per thread), stage it as two [32 queries][32 dims] boxes and reduce
+// them into dQ.
 // ---------------------------------------------------------------------------------------------
 struct Bw2Cfg {
     static constexpr int D = 128;
@@ -389,11 +390,12 @@ struct Bw2Cfg {
     static constexpr int OFF_K = 0, OFF_V = 32768;       // 128 keys x 128 dims bf16, two 64-column boxes
     static constexpr int OFF_RING = 65536;
     static constexpr int QD = 16384;                     // 64 rows x 128 dims bf16: two boxes of 8 KB
+    static constexpr int STAGES = 3;
     static constexpr int STAGE = 2 * QD + 1024;          // Q, dO, then lse2[64], dvec[64]
-    static constexpr int OFF_PT = OFF_RING + 2 * STAGE;  // P^T [128 keys][64 queries] bf16 (128 B rows)
+    static constexpr int OFF_PT = OFF_RING + STAGES * STAGE;  // P^T [128 keys][64 queries] bf16 (128 B rows)
     static constexpr int OFF_DST = OFF_PT + 16384;       // dS^T, same layout
-    static constexpr int OFF_DQS = OFF_DST + 16384;      // 4 warps x [64 queries][32 dims] fp32, swizzled
-    static constexpr int SMEM = 1024 + OFF_DQS + 4 * 8192;
+    static constexpr int OFF_DQS = OFF_DST + 16384;      // 4 warps x [32 queries][32 dims] fp32, swizzled
+    static constexpr int SMEM = 1024 + OFF_DQS + 4 * 4096;
     static constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 256, T_DK = 384;  // dQ^T: 2 x 64 columns
     static constexpr uint32_t IDESC_SD = idesc_f16(128, 64, 1, 1, 0, 0);   // S^T, dP^T: K-major A and B
     static constexpr uint32_t IDESC_KV = idesc_f16(128, 128, 1, 1, 0, 1);  // dV, dK: A K-major, B MN-major
@@ -410,8 +412,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     constexpr int D = C::D;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t bar_kv, bar_qdo_full[2], bar_qdo_empty[2], bar_s_full, bar_sdp_free,
-        bar_ps_full, bar_ps_empty, bar_dq_full[2], bar_dq_free[2], bar_done;
+    __shared__ __align__(8) uint64_t bar_kv, bar_qdo_full[Bw2Cfg::STAGES], bar_qdo_empty[Bw2Cfg::STAGES],
+        bar_s_full, bar_sdp_free, bar_ps_full, bar_ps_empty, bar_dq_full[2], bar_dq_free[2], bar_done;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
 
@@ -439,9 +441,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     }
     if (threadIdx.x == 0) {
         mbar_init(&bar_kv, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(&bar_qdo_full[i], 1);
             mbar_init(&bar_qdo_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_dq_full[i], 1);
             mbar_init(&bar_dq_free[i], 128);
         }
@@ -460,7 +464,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
     auto step_head = [&](int s) { return hk * p.group + s / n_i; };
     auto step_tile = [&](int s) { return i_first + s % n_i; };
-    auto stage_ptr = [&](int s) { return smem + C::OFF_RING + (s & 1) * C::STAGE; };
+    // step s uses ring stage s % 3 for the (s / 3)-th time: that use's barrier phase parity is (s / 3) & 1
+    auto stage_ptr = [&](int s) { return smem + C::OFF_RING + (s % C::STAGES) * C::STAGE; };
 
     if (warp == BW_TMA_WARP) {
         // ================================ TMA producer (one lane) ================================
@@ -472,8 +477,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             }
             int issued = 0;
             for (int s = 0; s < n_steps; ++s) {
-                const int st = s & 1;
-                if (s >= 2 && !mbar_wait(&bar_qdo_empty[st], ((s >> 1) - 1) & 1, limit_ns, &abort_flag)) {
+                const int st = s % C::STAGES;
+                if (s >= C::STAGES && !mbar_wait(&bar_qdo_empty[st], ((s / C::STAGES) - 1) & 1, limit_ns, &abort_flag)) {
                     bw_fail(&abort_flag, ERRBIT_WAIT_EMPTY);
                     break;
                 }
@@ -492,8 +497,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             if (abort_flag) {  // wait (bounded) for the copies in flight before the CTA may exit
                 volatile int never = 0;
                 (void)mbar_wait(&bar_kv, 0, limit_ns, &never);
-                for (int s = issued > 2 ? issued - 2 : 0; s < issued; ++s)
-                    (void)mbar_wait(&bar_qdo_full[s & 1], (s >> 1) & 1, limit_ns, &never);
+                for (int s = issued > C::STAGES ? issued - C::STAGES : 0; s < issued; ++s)
+                    (void)mbar_wait(&bar_qdo_full[s % C::STAGES], (s / C::STAGES) & 1, limit_ns, &never);
             }
         }
         __syncwarp();
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         for (int s = 0; s <= n_steps && ok; ++s) {
             if (s < n_steps) {
                 // ---- S^T(s) = K Q^T, dP^T(s) = V dO^T ----
-                if (!wait_all(&bar_qdo_full[s & 1], (s >> 1) & 1, ERRBIT_WAIT_Q)) { ok = false; break; }
+                if (!wait_all(&bar_qdo_full[s % C::STAGES], (s / C::STAGES) & 1, ERRBIT_WAIT_Q)) { ok = false; break; }
                 if (s > 0 && !wait_all(&bar_sdp_free, (s - 1) & 1, ERRBIT_WAIT_P)) { ok = false; break; }
                 tc_fence_after();
                 if (elect_one()) {
@@ -553,7 +558,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < C::QT / 16; ++kk)
                         umma_ss(tmem + C::T_DK, dDST_k + col16(kk), dQ_mn + rows16(kk), C::IDESC_KV, (t > 0 || kk > 0));
-                    umma_commit(&bar_qdo_empty[t & 1]);  // Q, dO of step t read: the stage may be refilled
+                    umma_commit(&bar_qdo_empty[t % C::STAGES]);  // Q, dO of step t read: the stage may be refilled
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T: contraction over the 128 keys
                         umma_ss(tmem + C::T_DQ + 64 * (t & 1), dK_mn + rows16(kk), dDST_n + rows16(kk), C::IDESC_Q, kk > 0);
@@ -578,10 +583,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const float sl = p.scale_log2;
         const uint32_t pt_row = smem_u32(smem + C::OFF_PT) + r * 128;
         const uint32_t dst_row = smem_u32(smem + C::OFF_DST) + r * 128;
-        const uint32_t stage = smem_u32(smem + C::OFF_DQS + wq * 8192);
+        const uint32_t stage = smem_u32(smem + C::OFF_DQS + wq * 4096);
         bool ok = true;
         // dQ of step t (warps 0-3): dQ^T from tensor memory (this thread: dimension 32 wq + lane, 64
-        // queries), staged as [64 queries][32 dims] (128-byte swizzled) and reduced into dQ
+        // queries), staged as two [32 queries][32 dims] boxes (128-byte swizzled) and reduced into dQ
         auto dq_out = [&](int t) -> bool {
             const bool got = mbar_wait(&bar_dq_full[t & 1], (t >> 1) & 1, limit_ns, &abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
@@ -596,22 +601,24 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             tmem_wait_ld(v1);
             tc_fence_before();
             mbar_arrive(&bar_dq_free[t & 1]);
-            if (lane == 0) bulk_wait_group_read<0>();  // the staging buffer's previous box was read
-            __syncwarp();
             const uint32_t colb = (lane & 3) * 4;
+            const int bh = b * p.H + step_head(t), it = step_tile(t);
 #pragma unroll
-            for (int q = 0; q < 64; ++q) {
-                const float val = __uint_as_float(q < 32 ? v0[q] : v1[q - 32]) * p.scale;
-                st_shared_f32(stage + q * 128 + ((((lane >> 2) ^ (q & 7))) << 4) + colb, val);
+            for (int hq = 0; hq < 2; ++hq) {  // queries 32 hq .. 32 hq + 31: one 32 x 32 box each
+                if (lane == 0) bulk_wait_group_read<0>();  // the staging buffer's previous box was read
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                    st_shared_f32(stage + q * 128 + ((((lane >> 2) ^ (q & 7))) << 4) + colb,
+                                  __uint_as_float(hq ? v1[q] : v0[q]) * p.scale);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {  // rows past N are not written by the reduction
+                    tma_reduce_add_3d(&tmDQ, smem + C::OFF_DQS + wq * 4096, wq * 32, it * C::QT + 32 * hq, bh);
+                    bulk_commit_group();
+                }
+                __syncwarp();
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {  // rows past N are not written by the reduction
-                const int bh = b * p.H + step_head(t), it = step_tile(t);
-                tma_reduce_add_3d(&tmDQ, smem + C::OFF_DQS + wq * 8192, wq * 32, it * C::QT, bh);
-                bulk_commit_group();
-            }
-            __syncwarp();
             return true;
         };
         for (int s = 0; s < n_steps && ok; ++s) {
@@ -620,7 +627,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             const float* lse2 = reinterpret_cast<const float*>(stage_ptr(s) + 2 * C::QD) + 32 * qh;
             const float* dvec = lse2 + 64;
             bool got = mbar_wait(&bar_s_full, s & 1, limit_ns, &abort_flag);
-            got = got && mbar_wait(&bar_qdo_full[s & 1], (s >> 1) & 1, limit_ns, &abort_flag);
+            got = got && mbar_wait(&bar_qdo_full[s % C::STAGES], (s / C::STAGES) & 1, limit_ns, &abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
                 if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_S);
                 ok = false;
