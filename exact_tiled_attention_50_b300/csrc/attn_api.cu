@@ -160,9 +160,9 @@ MapEntry g_map_cache[kMapCache];
 int g_map_next = 0;
 std::mutex g_map_mutex;
 
-// MAP_Q64_BF16: bf16 rows in boxes of 64 columns x 64 rows (the d = 128 backward's query tiles); the
-// others as described above.
-enum { MAP_Q_BF16 = 0, MAP_K_BF16 = 1, MAP_V_F16 = 2, MAP_O_F32 = 3, MAP_U8 = 4, MAP_Q64_BF16 = 5 };
+// MAP_Q64_BF16: bf16 rows in boxes of 64 columns x 64 rows; MAP_O16_F32: fp32 boxes of 32 columns x 16
+// rows (the d = 128 backward's query tiles and dQ reductions); the others as described above.
+enum { MAP_Q_BF16 = 0, MAP_K_BF16 = 1, MAP_V_F16 = 2, MAP_O_F32 = 3, MAP_U8 = 4, MAP_Q64_BF16 = 5, MAP_O16_F32 = 6 };
 
 bool encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int d, int rows, long long slabs,
                      unsigned box_rows);
@@ -180,7 +180,8 @@ bool get_map(CUtensorMap* m, int kind, const void* base, int d, int rows, long l
             }
     }
     bool ok = false;
-    if (kind == MAP_O_F32) ok = encode_out_map(m, const_cast<void*>(base), d, rows, slabs, 32);
+    if (kind == MAP_O_F32 || kind == MAP_O16_F32)
+        ok = encode_out_map(m, const_cast<void*>(base), d, rows, slabs, kind == MAP_O16_F32 ? 16 : 32);
     else if (kind == MAP_U8) ok = encode_u8_map(m, base, d, rows, slabs);
     else ok = encode_rows_map(m, base, kind == MAP_V_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                               d, rows, slabs, kind == MAP_Q64_BF16 ? 64 : 128);
@@ -486,7 +487,7 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const float* O
         !get_map(&tmK, MAP_K_BF16, K, d, N, static_cast<long long>(B) * H_kv) ||
         !get_map(&tmV, MAP_K_BF16, V, d, N, static_cast<long long>(B) * H_kv) ||
         !get_map(&tmDO, q64 ? MAP_Q64_BF16 : MAP_Q_BF16, dO, d, N, static_cast<long long>(B) * H) ||
-        !get_map(&tmDQ, MAP_O_F32, dQ, d, N, static_cast<long long>(B) * H))
+        !get_map(&tmDQ, q64 ? MAP_O16_F32 : MAP_O_F32, dQ, d, N, static_cast<long long>(B) * H))
         return ATTN_ERR_UNSUPPORTED;
 
     attn_impl::BwdPrepParams pp{};

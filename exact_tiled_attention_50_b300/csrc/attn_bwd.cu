@@ -380,9 +380,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 // (query tile i of one head of the group) the MMA warp issues S^T(s), dP^T(s) (M = 128 keys, N = 64
 // queries), then the second-phase products of step s - 1: dV += P^T dO, dK += dS^T Q (which release
 // the ring stage), dQ^T = K^T dS^T (M = d, N = 64 queries) into one of two TMEM buffers. Warps 0-7
-// compute P^T, dS^T (one key row per thread, 32 queries each); warps 0-3 then read dQ^T of the
-// previous step (one dimension per thread), stage it as two [32 queries][32 dims] boxes and reduce
-// them into dQ.
+// compute P^T, dS^T (one key row per thread, 32 queries each), then read dQ^T of the previous step
+// for the same 32 queries (one dimension per thread), stage it as two [16 queries][32 dims] boxes
+// and reduce them into dQ.
 // ---------------------------------------------------------------------------------------------
 struct Bw2Cfg {
     static constexpr int D = 128;
@@ -394,8 +394,8 @@ struct Bw2Cfg {
     static constexpr int STAGE = 2 * QD + 1024;          // Q, dO, then lse2[64], dvec[64]
     static constexpr int OFF_PT = OFF_RING + STAGES * STAGE;  // P^T [128 keys][64 queries] bf16 (128 B rows)
     static constexpr int OFF_DST = OFF_PT + 16384;       // dS^T, same layout
-    static constexpr int OFF_DQS = OFF_DST + 16384;      // 4 warps x [32 queries][32 dims] fp32, swizzled
-    static constexpr int SMEM = 1024 + OFF_DQS + 4 * 4096;
+    static constexpr int OFF_DQS = OFF_DST + 16384;      // 8 warps x [16 queries][32 dims] fp32, swizzled
+    static constexpr int SMEM = 1024 + OFF_DQS + 8 * 2048;
     static constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 256, T_DK = 384;  // dQ^T: 2 x 64 columns
     static constexpr uint32_t IDESC_SD = idesc_f16(128, 64, 1, 1, 0, 0);   // S^T, dP^T: K-major A and B
     static constexpr uint32_t IDESC_KV = idesc_f16(128, 128, 1, 1, 0, 1);  // dV, dK: A K-major, B MN-major
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_dq_full[i], 1);
-            mbar_init(&bar_dq_free[i], 128);
+            mbar_init(&bar_dq_free[i], 256);
         }
         mbar_init(&bar_s_full, 1);
         mbar_init(&bar_sdp_free, 256);
@@ -583,10 +583,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const float sl = p.scale_log2;
         const uint32_t pt_row = smem_u32(smem + C::OFF_PT) + r * 128;
         const uint32_t dst_row = smem_u32(smem + C::OFF_DST) + r * 128;
-        const uint32_t stage = smem_u32(smem + C::OFF_DQS + wq * 4096);
+        const uint32_t stage = smem_u32(smem + C::OFF_DQS + warp * 2048);
         bool ok = true;
-        // dQ of step t (warps 0-3): dQ^T from tensor memory (this thread: dimension 32 wq + lane, 64
-        // queries), staged as two [32 queries][32 dims] boxes (128-byte swizzled) and reduced into dQ
+        // dQ of step t for this warp's 32 queries: dQ^T from tensor memory (this thread: dimension
+        // 32 wq + lane), staged as two [16 queries][32 dims] boxes (128-byte swizzled), reduced into dQ
         auto dq_out = [&](int t) -> bool {
             const bool got = mbar_wait(&bar_dq_full[t & 1], (t >> 1) & 1, limit_ns, &abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
@@ -594,27 +594,26 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 return false;
             }
             tc_fence_after();
-            uint32_t v0[32], v1[32];
-            tmem_ld32(tmem + lane_off + C::T_DQ + 64 * (t & 1), v0);
-            tmem_ld32(tmem + lane_off + C::T_DQ + 64 * (t & 1) + 32, v1);
+            uint32_t v0[32];
+            tmem_ld32(tmem + lane_off + C::T_DQ + 64 * (t & 1) + 32 * qh, v0);
             tmem_wait_ld(v0);
-            tmem_wait_ld(v1);
             tc_fence_before();
             mbar_arrive(&bar_dq_free[t & 1]);
             const uint32_t colb = (lane & 3) * 4;
             const int bh = b * p.H + step_head(t), it = step_tile(t);
 #pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {  // queries 32 hq .. 32 hq + 31: one 32 x 32 box each
+            for (int hq = 0; hq < 2; ++hq) {  // queries 32 qh + 16 hq .. + 15: one 32 x 16 box each
                 if (lane == 0) bulk_wait_group_read<0>();  // the staging buffer's previous box was read
                 __syncwarp();
 #pragma unroll
-                for (int q = 0; q < 32; ++q)
+                for (int q = 0; q < 16; ++q)
                     st_shared_f32(stage + q * 128 + ((((lane >> 2) ^ (q & 7))) << 4) + colb,
-                                  __uint_as_float(hq ? v1[q] : v0[q]) * p.scale);
+                                  __uint_as_float(v0[16 * hq + q]) * p.scale);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {  // rows past N are not written by the reduction
-                    tma_reduce_add_3d(&tmDQ, smem + C::OFF_DQS + wq * 4096, wq * 32, it * C::QT + 32 * hq, bh);
+                    tma_reduce_add_3d(&tmDQ, smem + C::OFF_DQS + warp * 2048, wq * 32,
+                                      it * C::QT + 32 * qh + 16 * hq, bh);
                     bulk_commit_group();
                 }
                 __syncwarp();
@@ -677,16 +676,14 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             fence_proxy_async_smem();  // the MMAs read P^T and dS^T through the async proxy
             tc_fence_before();
             mbar_arrive(&bar_ps_full);
-            if (qh == 0 && s > 0 && !dq_out(s - 1)) {
+            if (s > 0 && !dq_out(s - 1)) {
                 ok = false;
                 break;
             }
         }
-        if (qh == 0) {
-            if (ok && n_steps > 0 && !dq_out(n_steps - 1)) ok = false;
-            if (lane == 0) bulk_wait_group_all();  // every reduction of this warp performed
-            __syncwarp();
-        }
+        if (ok && n_steps > 0 && !dq_out(n_steps - 1)) ok = false;
+        if (lane == 0) bulk_wait_group_all();  // every reduction of this warp performed
+        __syncwarp();
         // ---- dK, dV of this key tile (warps 0-3): fp32 rows straight to device memory ----
         if (qh == 0 && ok && n_steps > 0) {
             const bool got = mbar_wait(&bar_done, 0, limit_ns, &abort_flag);
