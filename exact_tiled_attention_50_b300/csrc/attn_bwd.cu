@@ -8,7 +8,9 @@
 //
 // Blackwell mapping: one CTA per (key tile of 128 keys, batch, kv head); it keeps K_j and V_j in
 // shared memory and accumulates dK_j and dV_j in tensor memory over every query head of its group and
-// every query tile (causal: the tiles at or after the key tile). Per query tile:
+// every query tile (causal: the tiles at or after the key tile). Two kernels share this mapping:
+// attn_bwd_tc_kernel (d = 64, query tiles of 128 rows, described here) and attn_bwd_q64_kernel
+// (d = 128, query tiles of 64 rows through a three-stage ring; described above it). Per query tile:
 //   MMA warp      S^T = K_j Q_i^T, dP^T = V_j dO_i^T         (TMEM cols 0-127, 128-255)
 //   warps 0-7     one key row each (warps 0-3 queries 0-63, warps 4-7 queries 64-127): P^T, dS^T ->
 //                 bf16 in shared memory (128-byte swizzled)
