@@ -233,9 +233,32 @@ def attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
                      kv_len: Optional[torch.Tensor] = None) -> None:
     """attn_fwd through the entry point that allocates nothing: the library's fixed device scratch
     replaces the workspace. q, k, v, out, lse (and kv_len) must already be contiguous CUDA tensors of
-    the shapes attn_fwd takes; this wrapper creates no tensor either."""
+    the shapes attn_fwd takes; this wrapper creates no tensor either, so it rejects (ValueError or
+    TypeError) what attn_fwd would have copied or converted instead of calling the library."""
+    tensors = {"q": q, "k": k, "v": v, "out": out, "lse": lse, "kv_len": kv_len}
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError(f"{name} must be a CUDA tensor on {q.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (this entry point makes no copies)")
+    if q.dim() != 4:
+        raise ValueError(f"q must be [B, H, N, d], got {tuple(q.shape)}")
     B, H, N, d = q.shape
-    H_kv = k.shape[1]
+    H_kv = k.shape[1] if k.dim() == 4 else -1
+    if k.shape != (B, H_kv, N, d) or v.shape != (B, H_kv, N, d):
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    _dtype_code(q.dtype)
+    if out.shape != (B, H, N, d):
+        raise ValueError(f"out must be [B, H, N, d] = {(B, H, N, d)}, got {tuple(out.shape)}")
+    _dtype_code(out.dtype)
+    if lse is not None and (lse.shape != (B, H, N) or lse.dtype != torch.float32):
+        raise ValueError(f"lse must be fp32 [B, H, N] = {(B, H, N)}")
+    if kv_len is not None and (kv_len.dtype != torch.int32 or kv_len.numel() != B):
+        raise ValueError("kv_len must be an int32 tensor of B elements")
     if scale is None:
         scale = d ** -0.5
     stream = torch.cuda.current_stream(q.device).cuda_stream

@@ -251,12 +251,17 @@ float attn_event_elapsed_ms(cudaEvent_t start, cudaEvent_t stop);
  * Arguments, layouts, results and errors are those of attn_fwd, without workspace/workspace_bytes.
  * The caller still allocates Q, K, V, O, LSE and kv_len. The scratch is a static device array of
  * ATTN_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library, which every GPU that loads the library
- * holds until the process exits. Sizes whose workspace (attn_workspace_bytes) exceeds it return
- * ATTN_ERR_UNSUPPORTED without launching; use attn_fwd with a workspace for those.
+ * holds until the process exits. The exact size limit: a call is accepted when
+ * attn_workspace_bytes(B, H, H_kv, N, d, ATTN_BF16) <= ATTN_NOALLOC_SCRATCH_BYTES (about 22.8 M
+ * elements of B * H_kv * N * d at d = 128, 28 M at d = 64); larger sizes return ATTN_ERR_UNSUPPORTED
+ * without launching (use attn_fwd with a workspace for those). fp32 inputs need no scratch.
  *
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
- * that device current); make that first call before any stream capture. No call allocates device
- * memory (no cudaMalloc, no cudaFree, no allocating library routine).
+ * that device current). With CUDA's lazy module loading (the default) that lookup is also what loads
+ * the library's device code on the device and so reserves the 64 MiB: make the first call on each
+ * device during initialisation, before memory pools are handed out and before any stream capture.
+ * The address is looked up again when the device's context changes (after cudaDeviceReset). No call
+ * allocates device memory (no cudaMalloc, no cudaFree, no allocating library routine).
  *
  * Every call on a device uses the same array, and the array keeps the contents of the last call.
  * Nothing in it needs clearing: each call writes every scratch byte it reads before reading it. Two
