@@ -7,10 +7,13 @@
 // log-sum-exp (safe_softmax_block listing of "AI训练的最大障碍不是算力,而是'内存墙'", zsdodo.com;
 // section 4.1.3 of "第四章 注意力机制实战案例", aiknowledge.cn).
 //
-// Mapping: a CTA of 128 threads owns 32 query rows of one (b, h); four consecutive lanes share a
-// row, each holding the query and output columns c = part + 4 i (interleaved, so that the four
-// lanes read consecutive shared-memory banks). Key/value tiles of 32 rows are staged in shared
-// memory with coalesced float4 loads.
+// Mapping: a CTA of 256 threads (8 warps) owns 8 query rows of one (b, h) and splits the key range
+// into 8 slices, one per warp, so that short sequences still spread over many warps: in a warp, four
+// consecutive lanes share a row and each holds a quarter of its query and output columns. Every warp
+// runs the online softmax over its slice (keys read straight from L2, 8 at a time); the 8 partial
+// results of a row are then combined in shared memory with the softmax merge rule (formula 2 of
+// "闪电注意力的数学原理" on the unite.ai page: m = max m_w, l = sum l_w e^(m_w - m), O = sum O_w
+// e^(m_w - m) / l).
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -20,24 +23,26 @@
 namespace attn_impl {
 
 namespace {
-constexpr int F32_ROWS = 32;
-constexpr int F32_KT = 32;
-constexpr int F32_THREADS = 128;
+constexpr int F32_ROWS = 8;      // query rows per CTA
+constexpr int F32_WARPS = 8;     // key slices per CTA
+constexpr int F32_THREADS = 32 * F32_WARPS;
+constexpr int F32_CHUNK = 8;     // keys per online-softmax update
 }  // namespace
 
 template <int D>
 __global__ void __launch_bounds__(F32_THREADS) attn_fwd_f32_kernel(const F32Params p) {
-    constexpr int CPT = D / 4;  // columns per thread
-    __shared__ __align__(16) float sK[F32_KT][D];
-    __shared__ __align__(16) float sV[F32_KT][D];
+    constexpr int CPL = D / 4;  // columns per lane
+    __shared__ __align__(16) float sm_o[F32_WARPS][F32_ROWS][D];
+    __shared__ float sm_m[F32_WARPS][F32_ROWS], sm_l[F32_WARPS][F32_ROWS];
+    __shared__ float sm_w[F32_WARPS][F32_ROWS], sm_inv[F32_ROWS], sm_lse[F32_ROWS];
 
     const int bh = blockIdx.y;
     const int b = bh / p.H, h = bh % p.H;
     const int kvh = h / p.group;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane >> 2, part = lane & 3;
     const int q_start = blockIdx.x * F32_ROWS;
-    const int tid = threadIdx.x;
-    const int part = tid & 3;
-    const int row = q_start + (tid >> 2);
+    const int row = q_start + r;
     const bool row_ok = row < p.N;
 
     int kv_valid = p.N;
@@ -45,71 +50,116 @@ __global__ void __launch_bounds__(F32_THREADS) attn_fwd_f32_kernel(const F32Para
         kv_valid = p.kv_len[b];
         kv_valid = kv_valid < 0 ? 0 : (kv_valid > p.N ? p.N : kv_valid);
     }
+    // keys any row of the CTA may attend to, split into one slice per warp
     const int limit = p.causal ? min(kv_valid, q_start + F32_ROWS) : kv_valid;
-    const int row_lim = p.causal ? min(kv_valid, row + 1) : kv_valid;
+    const int per_warp = (limit + F32_WARPS - 1) / F32_WARPS;
+    const int k_begin = warp * per_warp;
+    const int k_end = min(limit, k_begin + per_warp);
+    const int row_lim = p.causal ? min(kv_valid, row + 1) : kv_valid;  // keys < row_lim are valid
 
-    const float* Qp = p.Q + (static_cast<size_t>(bh) * p.N + (row_ok ? row : 0)) * D;
-    const float* Kp = p.K + (static_cast<size_t>(b) * p.H_kv + kvh) * static_cast<size_t>(p.N) * D;
-    const float* Vp = p.V + (static_cast<size_t>(b) * p.H_kv + kvh) * static_cast<size_t>(p.N) * D;
+    const float* Kp = p.K + (static_cast<size_t>(b) * p.H_kv + kvh) * static_cast<size_t>(p.N) * D + part * CPL;
+    const float* Vp = p.V + (static_cast<size_t>(b) * p.H_kv + kvh) * static_cast<size_t>(p.N) * D + part * CPL;
 
-    float q[CPT], o[CPT];
+    float q[CPL], o[CPL];
+    {
+        const float4* q4 = reinterpret_cast<const float4*>(
+            p.Q + (static_cast<size_t>(bh) * p.N + (row_ok ? row : 0)) * D + part * CPL);
 #pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-        q[i] = row_ok ? Qp[part + 4 * i] : 0.f;
-        o[i] = 0.f;
+        for (int i = 0; i < CPL / 4; ++i) {
+            const float4 v = row_ok ? __ldg(q4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            q[4 * i] = v.x; q[4 * i + 1] = v.y; q[4 * i + 2] = v.z; q[4 * i + 3] = v.w;
+        }
     }
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) o[i] = 0.f;
     float m = -INFINITY, l = 0.f;
 
-    for (int k0 = 0; k0 < limit; k0 += F32_KT) {
-        __syncthreads();
-        // stage K and V rows [k0, k0 + 32) (zero past N)
-        for (int idx = tid; idx < F32_KT * D / 4; idx += F32_THREADS) {
-            const int kr = idx / (D / 4), c4 = idx % (D / 4);
-            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-            if (k0 + kr < p.N) {
-                kv = reinterpret_cast<const float4*>(Kp + static_cast<size_t>(k0 + kr) * D)[c4];
-                vv = reinterpret_cast<const float4*>(Vp + static_cast<size_t>(k0 + kr) * D)[c4];
-            }
-            reinterpret_cast<float4*>(&sK[kr][0])[c4] = kv;
-            reinterpret_cast<float4*>(&sV[kr][0])[c4] = vv;
-        }
-        __syncthreads();
-        float s[F32_KT];
+    for (int k0 = k_begin; k0 < k_end; k0 += F32_CHUNK) {  // warp-uniform loop
+        float s[F32_CHUNK];
 #pragma unroll
-        for (int j = 0; j < F32_KT; ++j) {
+        for (int j = 0; j < F32_CHUNK; ++j) {
+            const int key = k0 + j;
             float acc = 0.f;
+            if (key < k_end) {
+                const float4* k4 = reinterpret_cast<const float4*>(Kp + static_cast<size_t>(key) * D);
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) acc = fmaf(q[i], sK[j][part + 4 * i], acc);
+                for (int i = 0; i < CPL / 4; ++i) {
+                    const float4 kv = __ldg(k4 + i);
+                    acc = fmaf(q[4 * i], kv.x, acc);
+                    acc = fmaf(q[4 * i + 1], kv.y, acc);
+                    acc = fmaf(q[4 * i + 2], kv.z, acc);
+                    acc = fmaf(q[4 * i + 3], kv.w, acc);
+                }
+            }
             acc += __shfl_xor_sync(0xffffffffu, acc, 1);
             acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            s[j] = (k0 + j < row_lim) ? acc * p.scale : -INFINITY;
+            s[j] = (key < k_end && key < row_lim) ? acc * p.scale : -INFINITY;
         }
         float mt = s[0];
 #pragma unroll
-        for (int j = 1; j < F32_KT; ++j) mt = fmaxf(mt, s[j]);
+        for (int j = 1; j < F32_CHUNK; ++j) mt = fmaxf(mt, s[j]);
         const float m_new = fmaxf(m, mt);
-        if (m_new == -INFINITY) continue;  // nothing valid for this row yet
+        // no valid key yet: m_new = -inf, every probability is 0 and o, l stay 0
         const float alpha = (m == -INFINITY) ? 0.f : expf(m - m_new);
-        float psum = 0.f;
+        l *= alpha;
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) o[i] *= alpha;
+        for (int i = 0; i < CPL; ++i) o[i] *= alpha;
 #pragma unroll
-        for (int j = 0; j < F32_KT; ++j) {
+        for (int j = 0; j < F32_CHUNK; ++j) {
             const float pj = (s[j] == -INFINITY) ? 0.f : expf(s[j] - m_new);
-            psum += pj;
+            l += pj;
+            if (k0 + j < k_end) {
+                const float4* v4 = reinterpret_cast<const float4*>(Vp + static_cast<size_t>(k0 + j) * D);
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) o[i] = fmaf(pj, sV[j][part + 4 * i], o[i]);
+                for (int i = 0; i < CPL / 4; ++i) {
+                    const float4 vv = __ldg(v4 + i);
+                    o[4 * i] = fmaf(pj, vv.x, o[4 * i]);
+                    o[4 * i + 1] = fmaf(pj, vv.y, o[4 * i + 1]);
+                    o[4 * i + 2] = fmaf(pj, vv.z, o[4 * i + 2]);
+                    o[4 * i + 3] = fmaf(pj, vv.w, o[4 * i + 3]);
+                }
+            }
         }
-        l = fmaf(alpha, l, psum);
         m = m_new;
     }
 
-    if (!row_ok) return;
-    float* Op = static_cast<float*>(p.O) + (static_cast<size_t>(bh) * p.N + row) * D;
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    // this warp's partial result of its slice: unnormalised O, m, l per row
 #pragma unroll
-    for (int i = 0; i < CPT; ++i) Op[part + 4 * i] = o[i] * inv;
-    if (p.LSE && part == 0) p.LSE[static_cast<size_t>(bh) * p.N + row] = (l > 0.f) ? m + logf(l) : -INFINITY;
+    for (int i = 0; i < CPL / 4; ++i)
+        reinterpret_cast<float4*>(&sm_o[warp][r][part * CPL])[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    if (part == 0) {
+        sm_m[warp][r] = l > 0.f ? m : -INFINITY;
+        sm_l[warp][r] = l;
+    }
+    __syncthreads();
+    // merge weights per (slice, row): e^(m_w - M) for slices with weight, 1 / L and the LSE per row
+    if (threadIdx.x < F32_ROWS) {
+        const int rr = threadIdx.x;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < F32_WARPS; ++w) M = fmaxf(M, sm_m[w][rr]);
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < F32_WARPS; ++w) {
+            const float wt = sm_l[w][rr] > 0.f ? expf(sm_m[w][rr] - M) : 0.f;
+            sm_w[w][rr] = wt;
+            L = fmaf(wt, sm_l[w][rr], L);
+        }
+        sm_inv[rr] = L > 0.f ? 1.f / L : 0.f;
+        sm_lse[rr] = L > 0.f ? M + logf(L) : -INFINITY;
+    }
+    __syncthreads();
+    float* Op = static_cast<float*>(p.O) + static_cast<size_t>(bh) * p.N * D;
+    for (int idx = threadIdx.x; idx < F32_ROWS * D; idx += F32_THREADS) {
+        const int rr = idx / D, c = idx % D;
+        if (q_start + rr >= p.N) continue;
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < F32_WARPS; ++w) acc = fmaf(sm_w[w][rr], sm_o[w][rr][c], acc);
+        Op[static_cast<size_t>(q_start + rr) * D + c] = acc * sm_inv[rr];
+    }
+    if (p.LSE && threadIdx.x < F32_ROWS && q_start + threadIdx.x < p.N)
+        p.LSE[static_cast<size_t>(bh) * p.N + q_start + threadIdx.x] = sm_lse[threadIdx.x];
 }
 
 cudaError_t launch_attn_f32(int d, const F32Params& p, cudaStream_t stream) {

@@ -27,8 +27,8 @@ enum : uint32_t {
 // number of 128-key steps it needs: the larger of its two tiles' key-tile counts below
 // min(kv_len[b], causal limit), and at least 1 (a unit without any valid key still writes O = 0,
 // LSE = -inf). Units lie on a line in (b, h, pair) order; unit u covers [off(u), off(u) + cost(u)).
-// CTA c of G first runs R_dp data-parallel rounds (unit r*G + c in round r; used only when every unit
-// has the same cost), then one contiguous chunk of the rest of the line,
+// CTA c of G first runs R_dp data-parallel rounds (unit r*G + c in round r, while that unit exists),
+// then, when the plan has a stream-K part (sk = 1), one contiguous chunk of the rest of the line,
 // [S0 + (W - S0) c / G, S0 + (W - S0) (c + 1) / G). A unit that a chunk boundary cuts is computed in
 // pieces over disjoint key ranges. The piece that holds the unit's first key step (the owner) is the
 // last segment of its CTA; the other pieces are the first segments of the following CTAs' chunks,
@@ -38,6 +38,9 @@ enum : uint32_t {
 // ---------------------------------------------------------------------------------------------
 constexpr int SCHED_MAX_CTAS = 160;  // partial-result slots reserved in the workspace
 constexpr int SCHED_MIN_STEPS = 2;   // the CTA count is capped so that chunks hold at least this many steps
+// Extra time of a split unit, in key steps: the owner waits for the later pieces' partial results and
+// reads them back before its epilogue. The plan splits units only when that saves more than this.
+constexpr int SCHED_SPLIT_PENALTY = 4;
 
 enum : int { SEG_COMPLETE = 0, SEG_OWNER = 1, SEG_WRITER = 2 };
 
@@ -62,8 +65,10 @@ __host__ __device__ inline int pair_cost(int pair, int nb, int N, int causal) {
 
 struct SchedPlan {
     int B, H, N, n_pairs, causal;
+    int units;      // B * H * n_pairs work units
     int G;          // persistent CTAs
-    int R_dp;       // data-parallel rounds
+    int R_dp;       // data-parallel rounds (the last one may be partial: units past `units` do not exist)
+    int sk;         // 1: a stream-K part follows the rounds; 0: every unit is whole (no partial results)
     int S0;         // line offset where the stream-K part starts (the whole line is below 2^31)
 };
 
@@ -71,7 +76,7 @@ struct Segment {
     int b, h, pair;
     int k0, k1;          // key steps [k0, k1) of the unit
     int cost;            // the unit's cost
-    int unit_end;        // line offset just past the unit
+    int unit_end;        // line offset just past the unit (stream-K segments; -1 in the rounds)
     int kind;            // SEG_COMPLETE, SEG_OWNER or SEG_WRITER
 };
 
@@ -130,8 +135,9 @@ __host__ __device__ inline void walk_locate(WalkState& w, const Tab& t, const Sc
 
 template <class Tab>
 __host__ __device__ inline bool walk_next(WalkState& w, const Tab& t, const SchedPlan& p, int cta, Segment& s) {
-    if (w.round < p.R_dp) {
-        const long long u = static_cast<long long>(w.round) * p.G + cta;
+    const long long u_dp = static_cast<long long>(w.round) * p.G + cta;
+    if (w.round < p.R_dp && u_dp < p.units) {
+        const long long u = u_dp;
         ++w.round;
         const long long per_b = static_cast<long long>(p.H) * p.n_pairs;
         s.b = static_cast<int>(u / per_b);
@@ -141,11 +147,12 @@ __host__ __device__ inline bool walk_next(WalkState& w, const Tab& t, const Sche
         s.cost = pair_cost(s.pair, nb, p.N, p.causal);
         s.k0 = 0;
         s.k1 = s.cost;
-        s.unit_end = static_cast<int>(t.boff(s.b)) + s.h * walk_head_cost(t, p, s.b) +
-                     static_cast<int>(pair_prefix(s.pair + 1, nb, p.N, p.causal));
+        s.unit_end = -1;  // read by owners of split units only; a round's unit is whole
         s.kind = SEG_COMPLETE;
         return true;
     }
+    w.round = p.R_dp;  // a partial last round ends the rounds of the CTAs past its end
+    if (!p.sk) return false;
     if (!w.sk_started) {
         w.sk_started = 1;
         w.pos = sched_chunk_start(p, w.W, cta);

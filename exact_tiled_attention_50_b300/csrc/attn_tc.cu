@@ -159,11 +159,17 @@ __device__ __forceinline__ int clamp_len(const int32_t* kv_len, int b, int N) {
 }  // namespace
 
 // Schedule table on the device: kv_len from the caller, batch offsets from the plan pass; reads the
-// kernel's grid-constant parameter in place.
+// kernel's grid-constant parameter in place. Without kv_len every batch costs the same, and the
+// offsets are computed here instead of read (no dependent global loads before the first tile).
 struct DevSchedTab {
     const TcParams& p;
     __device__ int nb(int b) const { return key_tiles(clamp_len(p.kv_len, b, p.plan.N)); }
-    __device__ long long boff(int b) const { return p.boff[b]; }
+    __device__ long long boff(int b) const {
+        if (p.kv_len == nullptr)
+            return static_cast<long long>(b) * p.plan.H *
+                   pair_prefix(p.plan.n_pairs, key_tiles(p.plan.N), p.plan.N, p.plan.causal);
+        return p.boff[b];
+    }
 };
 
 // Per-segment quantities every role derives the same way.
@@ -228,6 +234,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const DevSchedTab tab{p};
+    // The kernel may start while the pre-pass that precedes it on the stream still runs (programmatic
+    // dependent launch). What the pre-pass writes: the fp16 V copy and its tile exponents, the batch
+    // offsets and cleared flags of the schedule, and (fp8) every operand. With kv_len or fp8 the whole
+    // CTA waits for it here; otherwise only the roles that read its output wait (the K/V producer
+    // before its first V tile, the softmax warpgroups before their first tile exponent), so that the
+    // set-up, the schedule walk and the Q and first K loads overlap the pre-pass.
+    const bool dep_early = FP8 || p.kv_len != nullptr;
+    if (dep_early) grid_dep_wait();
     if (warp < 11 && lane == 0) walk_init(walk_sh[warp], tab, p.plan);
     // warp-collective: the next segment of this warp's walker into seg_sh[warp]
     auto next_seg = [&]() -> bool {
@@ -287,6 +301,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint32_t segk = 0;     // segments whose first K was issued
                 bool ok = true;
                 bool skip_k = p.debug_skip_kv_load != 0;  // failure-path test: the first K is never loaded
+                bool dep_done = dep_early;                  // the pre-pass's output may be read
                 while (ok && walk_next(walk, tab, p.plan, static_cast<int>(blockIdx.x), seg_sh[TMA_WARP])) {
                     const SegInfo si = seg_info(p, s);
                     if (si.nmax == 0) continue;
@@ -312,6 +327,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             break;
                         }
                         const bool has_k = j + 1 < jend;
+                        if (!dep_done) {  // the first V tile comes from the pre-pass
+                            grid_dep_wait();
+                            dep_done = true;
+                        }
                         mbar_arrive_expect_tx(&bar_full[st], has_k ? 2 * C::TILE_BYTES : C::TILE_BYTES);
                         uint8_t* dst = smem + C::OFF_RING + st * C::STAGE_BYTES;
                         if constexpr (FP8) {  // V^T tile: keys j*128.. (innermost), all d rows
@@ -511,6 +530,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         regs_increase<SOFTMAX_REGS>();
         // ============================ softmax warpgroups ============================
+        if (!dep_early) grid_dep_wait();  // tile exponents of V, flags of the schedule
         const int t = warp >> 2;            // query tile of this warpgroup
         const int wq = warp & 3;            // TMEM lane quarter
         const int r = wq * 32 + lane;       // row within the tile
@@ -1083,6 +1103,7 @@ constexpr int VPREP_THREADS = 256;
 constexpr int VPREP_VECS = 128 * 128 / 8 / VPREP_THREADS;  // 16-byte vectors per thread (d = 128)
 
 __global__ void __launch_bounds__(VPREP_THREADS) vprep_kernel(const VPrepParams p, const PlanParams pl) {
+    grid_dep_launch_dependents();  // the attention kernel may start its set-up on SMs this pass leaves
     const int tile = blockIdx.x, head = blockIdx.y;
     if (head == p.heads) {  // the extra row of blocks: block 0 plans, the others have nothing to do
         if (tile == 0) plan_block(pl);
@@ -1270,6 +1291,7 @@ __device__ void fp8_prep_v_tile(const __nv_bfloat16* src, uint8_t* dstT, int32_t
 }
 
 __global__ void __launch_bounds__(FP8P_THREADS) fp8_prep_kernel(const Fp8PrepParams p, const PlanParams pl) {
+    grid_dep_launch_dependents();
     __shared__ uint32_t red[FP8P_THREADS / 32];
     __shared__ uint16_t vt[128][130];
     const int tile = blockIdx.x, y = blockIdx.y;
@@ -1323,19 +1345,35 @@ static cudaError_t launch_tc_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, c
         if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
     }
     if (p.plan.G <= 0 || p.plan.G > SCHED_MAX_CTAS) return cudaErrorInvalidConfiguration;
-    // Cooperative launch: every CTA is resident at once, so an owner CTA may wait (bounded) for the
-    // partial results of the CTAs after it.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.plan.G));
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = Cfg<D, FP8>::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    // Programmatic dependent launch: the kernel may start while the pre-pass before it still runs (it
+    // waits for the pre-pass's output in the roles that read it).
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    // A plan that splits units needs every CTA resident at once (an owner CTA waits, bounded, for the
+    // partial results of the CTAs after it): cooperative launch. Whole-unit plans need no such guarantee.
+    if (p.plan.sk) {
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na].val.cooperative = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     e = cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, tmO, p);
+    if (e != cudaSuccess && na == 2) {
+        // a driver that refuses the combination: launch cooperatively without the early start
+        (void)cudaGetLastError();
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, tmO, p);
+    }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1387,16 +1425,39 @@ SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms) {
     p.causal = causal;
     p.n_pairs = (N + 2 * BLOCK_M - 1) / (2 * BLOCK_M);
     const long long units = static_cast<long long>(B) * H * p.n_pairs;
+    p.units = static_cast<int>(units);
     const int nb = key_tiles(N);
     const long long w_max = static_cast<long long>(B) * H * pair_prefix(p.n_pairs, nb, N, causal);
-    long long g = sms < SCHED_MAX_CTAS ? sms : SCHED_MAX_CTAS;
+    const long long g_cap = sms < SCHED_MAX_CTAS ? sms : SCHED_MAX_CTAS;
+    // Two plans, compared by the key steps of the busiest CTA (kv_len counts as N: an upper bound).
+    // Stream-K: G CTAs share the line evenly, units cut by chunk boundaries pay the merge penalty.
+    long long g = g_cap;
     const long long g_steps = (w_max + SCHED_MIN_STEPS - 1) / SCHED_MIN_STEPS;
     if (g_steps < g) g = g_steps;
     if (g < 1) g = 1;
+    const long long t_stream = (w_max + g - 1) / g + SCHED_SPLIT_PENALTY;
+    // Whole units in rounds (unit r * G + c on CTA c): with equal costs every CTA runs ceil(units / G)
+    // of them; with unequal costs (causal or kv_len) only one round is considered, bounded by the
+    // costliest unit.
+    const bool uniform = !causal && !has_kv_len;
+    long long max_cost = 1;
+    for (int pr = 0; pr < p.n_pairs; ++pr) {
+        const long long c = pair_cost(pr, nb, N, causal);
+        if (c > max_cost) max_cost = c;
+    }
+    const long long rounds = (units + g_cap - 1) / g_cap;
+    const long long t_whole = uniform ? rounds * nb : (rounds == 1 ? max_cost : -1);
+    if (t_whole >= 0 && t_whole <= t_stream) {
+        p.R_dp = static_cast<int>(rounds);
+        p.G = static_cast<int>((units + rounds - 1) / rounds);  // the fewest CTAs for that many rounds
+        p.sk = 0;
+        p.S0 = static_cast<int>(w_max);  // unused: no stream-K part
+        return p;
+    }
     p.G = static_cast<int>(g);
+    p.sk = 1;
     // data-parallel rounds only when every unit costs the same; the last one or two rounds' worth of
     // units go to the balanced stream-K part
-    const bool uniform = !causal && !has_kv_len;
     const long long r = uniform ? units / g - 1 : 0;
     p.R_dp = r > 0 ? static_cast<int>(r) : 0;
     p.S0 = static_cast<int>(static_cast<long long>(p.R_dp) * p.G * nb);

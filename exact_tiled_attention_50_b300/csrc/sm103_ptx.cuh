@@ -373,6 +373,18 @@ __device__ __forceinline__ bool flag_wait(const unsigned int* f, unsigned int v,
 }
 
 // ---------------------------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation may start
+// while the kernel before it on the stream still runs. It waits for that kernel's completion (and
+// the visibility of its writes) with grid_dep_wait before touching anything the earlier kernel
+// writes; the earlier kernel lets it start early with grid_dep_launch_dependents. Without the launch
+// attribute both are no-ops.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
 // Misc
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {

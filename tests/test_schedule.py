@@ -82,6 +82,14 @@ def test_schedule_covers_every_key_step_once(attn, B, H, N, causal, kv_len, sms)
             assert all(p[3] == WRITER for p in pieces[1:])
 
 
+SPLIT_PENALTY = 4  # key steps a split unit costs its owner (the plan's cost model)
+
+
+def plan_kind(segs):
+    """'stream' when some unit is computed in pieces (or the plan could split), 'whole' otherwise."""
+    return "stream" if any(s[7] != COMPLETE for s in segs) else "whole"
+
+
 @pytest.mark.parametrize("B,H,N,causal,kv_len,sms", CASES)
 def test_schedule_roles_and_balance(attn, B, H, N, causal, kv_len, sms):
     segs = attn.schedule(B, H, N, causal, kv_len, sms)
@@ -97,9 +105,58 @@ def test_schedule_roles_and_balance(attn, B, H, N, causal, kv_len, sms):
             assert all(k == COMPLETE for k in kinds[:kinds.index(WRITER)])
         assert kinds.count(OWNER) <= 1 and (OWNER not in kinds or kinds[-1] == OWNER)
         load.append(sum(s[5] - s[4] for s in lst))
-    total = sum(load)
-    # every CTA gets the mean load up to rounding (whole data-parallel units weigh the same)
-    assert max(load) - min(load) <= 1, (min(load), max(load), total / G)
+    assert min(load) >= 1  # no CTA is launched without work
+    n_pairs = math.ceil(N / 256)
+    units = B * H * n_pairs
+    if plan_kind(segs) == "stream":
+        # every CTA gets the mean load up to rounding (whole data-parallel units weigh the same)
+        assert max(load) - min(load) <= 1, (min(load), max(load), sum(load) / G)
+    else:
+        # whole units in rounds: unit r * G + c on CTA c, no CTA idle in the first round
+        assert G == math.ceil(units / math.ceil(units / G))
+        for c, lst in per_cta.items():
+            us = [(s[1] * H + s[2]) * n_pairs + s[3] for s in lst]
+            assert us == list(range(c, units, G))
+
+
+def model_makespans(B, H, N, causal, padded, sms):
+    """Busiest CTA's key steps under each plan (kv_len counted as N), as the plan's cost model states."""
+    nb = math.ceil(N / 128)
+    n_pairs = math.ceil(N / 256)
+    costs = [unit_cost(N, causal, N, p) for p in range(n_pairs)]
+    w = B * H * sum(costs)
+    g_cap = min(sms, 160)
+    g = max(1, min(g_cap, math.ceil(w / 2)))
+    t_stream = math.ceil(w / g) + SPLIT_PENALTY
+    units = B * H * n_pairs
+    rounds = math.ceil(units / g_cap)
+    uniform = not causal and not padded
+    t_whole = rounds * nb if uniform else (max(costs) if rounds == 1 else None)
+    return t_whole, t_stream
+
+
+@pytest.mark.parametrize("B,H,N,causal,kv_len,sms", CASES)
+def test_schedule_takes_the_cheaper_plan(attn, B, H, N, causal, kv_len, sms):
+    segs = attn.schedule(B, H, N, causal, kv_len, sms)
+    t_whole, t_stream = model_makespans(B, H, N, causal, kv_len is not None, sms)
+    want = "whole" if t_whole is not None and t_whole <= t_stream else "stream"
+    got = plan_kind(segs)
+    # a stream-K plan whose chunk boundaries all fall on unit boundaries splits nothing: it looks whole
+    assert got == want or (want == "stream" and got == "whole")
+
+
+@pytest.mark.parametrize("B,H,N,causal,kv_len,expect_G,expect", [
+    (4, 8, 1024, False, None, 128, "whole"),       # 128 units of 8 steps: one round, no merges
+    (1, 16, 512, False, None, 32, "whole"),        # 32 units of 4 steps
+    (1, 16, 512, True, None, 32, "whole"),
+    (1, 16, 8192, False, None, 148, "stream"),     # 512 units of 64 steps: 3.46 rounds -> stream-K
+    (1, 16, 16384, False, None, 148, "stream"),
+    (2, 32, 8192, True, None, 148, "stream"),
+])
+def test_schedule_choice_on_the_workloads(attn, B, H, N, causal, kv_len, expect_G, expect):
+    segs = attn.schedule(B, H, N, causal, kv_len, 148)
+    assert max(s[0] for s in segs) + 1 == expect_G
+    assert plan_kind(segs) == expect
 
 
 def test_schedule_rejects_bad_arguments(attn):
