@@ -8,6 +8,11 @@ workload, inputs resident in HBM. Default workload: B=1, H=16, N=8192, d=128, bf
 every timed step, outside the timed events. Under torchrun each rank runs the same workload on its
 own GPU (independent problems, no collective on the data path) and the max time over ranks counts.
 
+The line also carries ``extras`` (skip with ``--no-extras``): the fp8, backward, bias + dropout and
+dropout paths timed on the same workload, the device time of one call of every workload (replayed
+from a CUDA graph, so that host launch overhead is not in it), and the oracle on one host core for
+the two smallest workloads.
+
 ``--impl reference`` times the fp64 CPU oracle instead (the only reference implementation available:
 the pages ship no runnable code), on a bounded sample of the workload's query rows per step.
 """
@@ -222,74 +227,91 @@ def run_reference(args, w):
     return 0
 
 
-def run_ours(args, w):
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    from exact_tiled_attention_50_b300 import attn
+def _path_meta(path):
+    """(metric, FLOP multiplier over the forward's nominal FLOPs, peak multiplier over the bf16 peak)."""
+    return {"bf16": (METRIC, 1.0, 1.0), "fp8": (METRIC_FP8, 1.0, 2.0), "bias_dropout": (METRIC_EX, 1.0, 1.0),
+            "dropout": (METRIC_EX, 1.0, 1.0), "bwd": (METRIC_BWD, 2.5, 1.0)}[path]
 
-    x = inputs.make_inputs(w)
-    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
-    kv = x.kv_len.to(dev) if x.kv_len is not None else None
-    B, H, N, d = q.shape
-    out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    fp8 = args.path == "fp8"
-    ex = args.path in ("bias_dropout", "dropout")
-    bias = None
-    if fp8:
-        wsb = int(attn.lib.attn_fwd_fp8_workspace_bytes(B, w.H, w.H_kv, N, d))
-        signs = inputs.random_signs(d, seed=0).to(dev)
-    else:
-        wsb = attn.workspace_bytes(B, w.H, w.H_kv, N, d, q.dtype)
-    if args.path == "bias_dropout":  # one bf16 bias value per (b, h, i, j), drawn on the device
-        gen = torch.Generator(device=dev)
-        gen.manual_seed(inputs.SEED_BASE + 4000)
-        bias = torch.randn((B, w.H, N, N), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
-    work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
-    bwd = args.path == "bwd"
-    if bwd:  # the forward's O and LSE once, and a seeded upstream gradient
-        attn.attn_fwd(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, out=out, lse=lse, workspace=work)
-        gen = torch.Generator().manual_seed(inputs.SEED_BASE + 5000)
-        dO = torch.randn(tuple(q.shape), generator=gen).to(torch.bfloat16).to(dev)
-    grads = []
+PATH_DESC = {"fp8": "fp8: Q, K rotated (random signs) + E4M3 per 128-row tile; E4M3 tensor cores",
+             "bias_dropout": "bf16 + additive bf16 bias [B,H,N,N] + dropout p=0.1 (Philox4x32-10)",
+             "dropout": "bf16 + dropout p=0.1 (Philox4x32-10)",
+             "bwd": "backward: dQ, dK, dV (fp32) from bf16 Q, K, V, dO and the forward's O, LSE",
+             "bf16": "bf16 tensor cores (fp16 P, fp16 V)"}
 
-    def step():
-        if bwd:
-            grads[:] = attn.attn_bwd(q, k, v, out, dO, lse, scale=x.scale, causal=w.causal, kv_len=kv)
-        elif fp8:
-            attn.attn_fwd_fp8(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, signs=signs, out=out, lse=lse,
-                              workspace=work)
-        elif ex:
-            attn.attn_fwd_ex(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, bias=bias, dropout_p=0.1, seed=1,
-                             offset=0, out=out, lse=lse, workspace=work)
+
+class Problem:
+    """Device tensors of one workload and the step of each path over them (every step one call of the
+    library's public API on the current stream, inputs resident)."""
+
+    def __init__(self, attn, w, x, dev):
+        self.attn, self.w, self.x, self.dev = attn, w, x, dev
+        self.q, self.k, self.v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        self.kv = x.kv_len.to(dev) if x.kv_len is not None else None
+        B, H, N, d = self.q.shape
+        self.out = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        wsb = max(attn.workspace_bytes(B, w.H, w.H_kv, N, d, self.q.dtype),
+                  int(attn.lib.attn_fwd_fp8_workspace_bytes(B, w.H, w.H_kv, N, d)) if d == 128 else 0)
+        self.work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+        self.bias = None
+        self.dO = None
+        self.grads = []
+
+    def prepare(self, path):
+        w, attn = self.w, self.attn
+        if path == "bias_dropout" and self.bias is None:  # one bf16 bias value per (b, h, i, j), drawn on the device
+            gen = torch.Generator(device=self.dev)
+            gen.manual_seed(inputs.SEED_BASE + 4000)
+            self.bias = torch.randn((w.B, w.H, w.N, w.N), generator=gen, device=self.dev,
+                                    dtype=torch.float32).to(torch.bfloat16)
+        if path == "fp8":
+            self.signs = inputs.random_signs(w.d, seed=0).to(self.dev)
+        if path == "bwd" and self.dO is None:  # the forward's O and LSE once, and a seeded upstream gradient
+            attn.attn_fwd(self.q, self.k, self.v, scale=self.x.scale, causal=w.causal, kv_len=self.kv, out=self.out,
+                          lse=self.lse, workspace=self.work)
+            gen = torch.Generator().manual_seed(inputs.SEED_BASE + 5000)
+            self.dO = torch.randn(tuple(self.q.shape), generator=gen).to(torch.bfloat16).to(self.dev)
+
+    def step_fn(self, path):
+        self.prepare(path)
+        attn, x, w = self.attn, self.x, self.w
+        q, k, v, kv, out, lse, work = self.q, self.k, self.v, self.kv, self.out, self.lse, self.work
+        if path == "bwd":
+            def step():
+                self.grads[:] = attn.attn_bwd(q, k, v, out, self.dO, lse, scale=x.scale, causal=w.causal, kv_len=kv)
+        elif path == "fp8":
+            def step():
+                attn.attn_fwd_fp8(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, signs=self.signs, out=out,
+                                  lse=lse, workspace=work)
+        elif path in ("bias_dropout", "dropout"):
+            bias = self.bias if path == "bias_dropout" else None
+
+            def step():
+                attn.attn_fwd_ex(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, bias=bias, dropout_p=0.1,
+                                 seed=1, offset=0, out=out, lse=lse, workspace=work)
         else:
-            attn.attn_fwd(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, out=out, lse=lse, workspace=work)
+            def step():
+                attn.attn_fwd(q, k, v, scale=x.scale, causal=w.causal, kv_len=kv, out=out, lse=lse, workspace=work)
+        return step
 
-    for _ in range(args.warmup):
+
+def timed_steps(attn, step, flush, stream, K, warmup, world=1):
+    """Per-step device times (ms) of K steps and of the library's main kernel inside each (CUDA events
+    on the launching stream; the L2 flush runs before each step, outside the events)."""
+    for _ in range(warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     rc = attn.check()
     if rc != attn.ATTN_OK:
         raise RuntimeError(f"warm-up failed: {attn.status_string(rc)}")
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for a, b in kev:  # torch creates the CUDA event on first record: materialise the handles now
         a.record(stream)
         b.record(stream)
-    if ws > 1:
+    if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
@@ -302,22 +324,149 @@ def run_ours(args, w):
     attn.set_kernel_events(None, None)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    clocks = sampler.stop()
     rc = attn.check()
     if rc != attn.ATTN_OK:
         raise RuntimeError(f"timed run failed: {attn.status_string(rc)}")
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    kern_ms = sum(attn.event_elapsed_ms(a, b) for a, b in kev) / K
-    step_ms, kern_ms = max_over_ranks([step_ms, kern_ms], device=dev)
+    return [a.elapsed_time(b) for a, b in ev], [attn.event_elapsed_ms(a, b) for a, b in kev], wall
 
-    # ---- end to end through the public API: pinned host inputs -> device -> attn_fwd -> host ----
+
+def graph_call_times(attn, step, flush, stream, reps=20, warmup=3):
+    """Device time (ms) of one call replayed from a CUDA graph, so that the host's launch overhead is
+    not in it: events before and after each replay, L2 flushed before each (outside the events)."""
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    cs = torch.cuda.Stream(stream.device)
+    cs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cs):
+        step()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    rc = attn.check()
+    if rc != attn.ATTN_OK:
+        raise RuntimeError(f"graph replay failed: {attn.status_string(rc)}")
+    del g
+    return ts
+
+
+def roofline_of(path, w, kern_ms, prob, peaks):
+    metric, fmul, pmul = _path_meta(path)
+    flops = flops_of(w) * fmul
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    peak = peaks["bf16"] * pmul
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak}
+    if path == "bias_dropout":
+        # the bias (2 B per score) outweighs the tensor work at these sizes: the kernel is HBM-bound
+        nbytes = (prob.bias.numel() * 2 + (prob.q.numel() + prob.k.numel() + prob.v.numel()) * 2 +
+                  prob.out.numel() * 4 + prob.lse.numel() * 4)
+        gbs = nbytes / (kern_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                "algorithmic_bytes": nbytes, "tensor_tflops": achieved}
+    return roof
+
+
+def run_extras(attn, prob, flush, stream, peaks, args):
+    """Other numbers on the same box in the same run: the other paths on the headline workload, the
+    device time of one call of every workload (graph replay, L2 flushed), and the oracle on one host
+    core for the two smallest workloads."""
+    extras = {}
+    paths = {}
+    for path in ("fp8", "bwd", "bias_dropout", "dropout"):
+        if path == "fp8" and prob.w.d != 128:
+            continue
+        step = prob.step_fn(path)
+        st, kt, _ = timed_steps(attn, step, flush, stream, args.extra_steps, 3)
+        metric, fmul, pmul = _path_meta(path)
+        flops = flops_of(prob.w) * fmul
+        km = statistics.median(kt)
+        roof = roofline_of(path, prob.w, km, prob, peaks)
+        paths[path] = {"metric": metric, "path": PATH_DESC[path], "steps": len(st),
+                       "ms_per_step_median": statistics.median(st), "ms_per_step_mean": sum(st) / len(st),
+                       "value": flops / (statistics.median(st) * 1e-3) / 1e12, "unit": UNIT,
+                       "kernel_ms_median": km, "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit",
+                                                                                 "frac")}}
+    prob.bias = None
+    prob.grads[:] = []
+    torch.cuda.empty_cache()
+    extras["paths"] = paths
+    wl = {}
+    for name, w in inputs.WORKLOADS.items():
+        x = inputs.make_inputs_device(w, prob.dev)
+        p2 = Problem(attn, w, x, prob.dev)
+        ts = graph_call_times(attn, p2.step_fn("bf16"), flush, stream)
+        med = statistics.median(ts)
+        lens = None if x.kv_len is None else x.kv_len.cpu().tolist()
+        wl[name] = {"us_per_call_median": med * 1e3, "tflops_nominal": w.nominal_flops() / (med * 1e-3) / 1e12,
+                    "tflops_effective": inputs.effective_flops(w, lens) / (med * 1e-3) / 1e12,
+                    "frac_of_bf16_peak": w.nominal_flops() / (med * 1e-3) / 1e12 / peaks["bf16"]}
+        del p2, x
+    torch.cuda.empty_cache()
+    extras["workloads"] = {"how": "one attn_fwd call (all its launches) captured in a CUDA graph, replayed 20 times, "
+                                  "median of the device time between events around each replay, L2 flushed before "
+                                  "each; inputs drawn on the device with the workload's recipe",
+                           "per_workload": wl}
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.num_threads()
+        oracle.set_num_threads(1)
+        one = {}
+        for name, frac in (("tiny_b1h1_n256_d64_f32", 1), ("b4h8_n1024_d64", 8)):
+            w = inputs.WORKLOADS[name]
+            x = inputs.make_inputs(w)
+            total = w.B * w.H * w.N
+            r = time_oracle(x, w, total // frac, 1, 0)
+            one[name] = {"value": r["value"], "unit": UNIT, "cores": 1, "kind": "oracle", "sample": r["sample"]}
+        oracle.set_num_threads(threads)
+        extras["cpu_baseline_1thread"] = one
+    return extras
+
+
+def run_ours(args, w):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from exact_tiled_attention_50_b300 import attn
+
+    x = inputs.make_inputs(w)
+    prob = Problem(attn, w, x, dev)
+    q, kv, out, lse = prob.q, prob.kv, prob.out, prob.lse
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    bwd = args.path == "bwd"
+    step = prob.step_fn(args.path)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    K = args.steps
+    st, kt, wall = timed_steps(attn, step, flush, stream, K, args.warmup, ws)
+    clocks = sampler.stop()
+    step_ms, kern_ms = sum(st) / K, sum(kt) / K
+    step_med, kern_med = statistics.median(st), statistics.median(kt)
+    step_ms, kern_ms, step_med, kern_med = max_over_ranks([step_ms, kern_ms, step_med, kern_med], device=dev)
+
+    # ---- end to end through the public API: pinned host inputs -> device -> the call -> host ----
     hq, hk, hv = x.q.pin_memory(), x.k.pin_memory(), x.v.pin_memory()
     hkv = x.kv_len.pin_memory() if x.kv_len is not None else None
     ho = torch.empty_like(out, device="cpu").pin_memory()
     hl = torch.empty_like(lse, device="cpu").pin_memory()
     # the backward's extra inputs (dO, and O, LSE of the forward) and its three gradients
-    h_in = [(dO.cpu().pin_memory(), dO), (ho, out), (hl, lse)] if bwd else []
-    h_grads = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in grads] if bwd else []
+    h_in = [(prob.dO.cpu().pin_memory(), prob.dO), (ho, out), (hl, lse)] if bwd else []
+    h_grads = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in prob.grads] if bwd else []
     e2e_steps = max(1, min(K, args.e2e_steps))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -325,16 +474,16 @@ def run_ours(args, w):
     for i in range(e2e_steps + 1):
         flush.zero_()
         e0.record(stream)
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
+        prob.q.copy_(hq, non_blocking=True)
+        prob.k.copy_(hk, non_blocking=True)
+        prob.v.copy_(hv, non_blocking=True)
         if hkv is not None:
             kv.copy_(hkv, non_blocking=True)
         for h, dvc in h_in:
             dvc.copy_(h, non_blocking=True)
         step()
         if bwd:
-            for h, g in zip(h_grads, grads):
+            for h, g in zip(h_grads, prob.grads):
                 h.copy_(g, non_blocking=True)
         else:
             ho.copy_(out, non_blocking=True)
@@ -349,53 +498,45 @@ def run_ours(args, w):
         (hkv.numel() * 4 if hkv is not None else 0)
     d2h = sum(t.numel() * t.element_size() for t in h_grads) if bwd else ho.numel() * 4 + hl.numel() * 4
 
-    # backward: 5 products of the forward's size (recomputed S, dP, dV, dK, dQ) against its 2
-    flops = flops_of(w) * (2.5 if bwd else 1.0)
+    metric, fmul, pmul = _path_meta(args.path)
+    flops = flops_of(w) * fmul
+    lens = None if x.kv_len is None else x.kv_len.tolist()
+    eff = inputs.effective_flops(w, lens) * fmul
     peaks = load_peaks()
-    achieved = flops / (kern_ms * 1e-3) / 1e12
-    # the contraction's own dtype: E4M3 takes the measured bf16 peak times the nominal fp8 / bf16 ratio
-    # (4.5 / 2.25 PFLOP/s dense)
-    peak = peaks["bf16"] * (2.0 if fp8 else 1.0)
-    peak_sus = peaks["bf16_sustained"] * (2.0 if fp8 else 1.0)
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak}
-    if bias is not None:
-        # the bias (2 B per score) outweighs the tensor work at these sizes: the kernel is HBM-bound
-        nbytes = (bias.numel() * 2 + (q.numel() + k.numel() + v.numel()) * 2 + out.numel() * 4 + lse.numel() * 4)
-        gbs = nbytes / (kern_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
-                "algorithmic_bytes": nbytes, "tensor_tflops": achieved}
+    roof = roofline_of(args.path, w, kern_ms, prob, peaks)
+    peak_sus = peaks["bf16_sustained"] * pmul
+    fp8 = args.path == "fp8"
+    ex = args.path in ("bias_dropout", "dropout")
     line = {
-        "metric": {"fp8": METRIC_FP8, "bias_dropout": METRIC_EX, "dropout": METRIC_EX,
-                   "bwd": METRIC_BWD}.get(args.path, METRIC),
+        "metric": metric,
         "value": job_value(flops, ws, step_ms),
         "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
+        "ms_per_step_median": step_med,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1), 1% of key rows x8)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d, "causal": w.causal,
-                   "in": "bf16", "out": "fp32 O + fp32 LSE",
-                   "path": {"fp8": "fp8: Q, K rotated (random signs) + E4M3 per 128-row tile; E4M3 tensor cores",
-                            "bias_dropout": "bf16 + additive bf16 bias [B,H,N,N] + dropout p=0.1 (Philox4x32-10)",
-                            "dropout": "bf16 + dropout p=0.1 (Philox4x32-10)",
-                            "bwd": "backward: dQ, dK, dV (fp32) from bf16 Q, K, V, dO and the forward's O, LSE"
-                            }.get(args.path,
-                                                                                  "bf16 tensor cores (fp16 P, fp16 V)"),
+                   "in": "bf16", "out": "fp32 O + fp32 LSE", "path": PATH_DESC[args.path],
                    "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
                    **({"bias": "bf16 [B,H,N,N] resident on the device (not part of the e2e copies)"}
-                      if bias is not None else {}),
+                      if args.path == "bias_dropout" else {}),
                    "parallelism": f"replicas x{ws} (independent problems per GPU)",
                    "pct_of_peak_bf16": 100.0 * flops / (step_ms * 1e-3) / 1e12 / peaks["bf16"]},
+        "effective": {"flops_per_step": eff, "nominal_flops_per_step": flops,
+                      "value": job_value(eff, ws, step_ms), "unit": UNIT,
+                      "note": "4 d per unmasked (query, key) pair (x2.5 for the backward)"},
         "roofline": {**roof,
                      "traffic": args.traffic if args.traffic is not None else profiled_traffic(w, args.path),
                      "kernel": (("attn_bwd_q64_kernel" if w.d == 128 else f"attn_bwd_tc_kernel<{w.d}>")
                                 + " (with its row-statistics pass)") if bwd
                      else f"attn_fwd_tc_kernel<{w.d},false,{1 if fp8 else 2 if ex else 0}>", "kernel_ms": kern_ms,
+                     "kernel_ms_median": kern_med,
                      "peak_source": (f"{peaks['source']} bf16 burst (cuBLAS) x 2 (nominal fp8/bf16 dense ratio)"
-                                     if fp8 else f"{peaks['source']} " + ("copy bandwidth" if bias is not None
+                                     if fp8 else f"{peaks['source']} " + ("copy bandwidth" if args.path == "bias_dropout"
                                                                           else "bf16 burst (cuBLAS)"))
-                                    + f"; tensor frac of sustained {achieved / peak_sus:.3f}"},
+                                    + f"; tensor frac of sustained {flops / (kern_ms * 1e-3) / 1e12 / peak_sus:.3f}"},
         "e2e": {"value": job_value(flops, ws, e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
-        "gpu_launches": K * attn.launches_per_call(q.dtype),
+        "gpu_launches": K * (2 if bwd else attn.launches_per_call(q.dtype)),
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
@@ -403,6 +544,8 @@ def run_ours(args, w):
         r = time_oracle(x, w, args.cpu_rows, 1, 0)
         line["cpu_baseline"] = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                                 "sample": r["sample"]}
+    if rank == 0 and ws == 1 and args.path == "bf16" and not args.no_extras:
+        line["extras"] = run_extras(attn, prob, flush, stream, peaks, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -422,6 +565,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--traffic", type=float, default=None, help="DRAM bytes per launch from an ncu capture")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other paths, the per-workload device times and the one-core oracle timings")
+    ap.add_argument("--extra-steps", type=int, default=20, help="timed steps of each other path in the extras")
     ap.add_argument("--path", choices=["bf16", "fp8", "bias_dropout", "dropout", "bwd"], default="bf16",
                     help="bf16 tensor-core path (the headline) or the fp8 path with incoherent processing")
     args = ap.parse_args()

@@ -117,6 +117,41 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> Inputs:
     return Inputs(q.contiguous(), k.contiguous(), v.contiguous(), kv_len, w.scale, w.causal)
 
 
+def make_inputs_device(w: Workload, device, seed: Optional[int] = None) -> Inputs:
+    """The recipe of ``make_inputs`` drawn on the device (a CUDA generator seeded the same way): the same
+    shapes, distributions and structure, a different stream of numbers. For timing large workloads
+    without drawing them on the host; parity always uses ``make_inputs``."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed if seed is None else seed)
+    dt = _DT[w.dtype]
+    q = torch.randn((w.B, w.H, w.N, w.d), generator=g, dtype=torch.float32, device=device).to(dt)
+    k = torch.randn((w.B, w.H_kv, w.N, w.d), generator=g, dtype=torch.float32, device=device).to(dt)
+    v = torch.randn((w.B, w.H_kv, w.N, w.d), generator=g, dtype=torch.float32, device=device).to(dt)
+    kv_len = None
+    if w.padded:
+        kv_len = torch.randint(w.N // 2, w.N + 1, (w.B,), generator=g, dtype=torch.int64, device=device).to(torch.int32)
+    if w.peaky:
+        n_rows = math.ceil(0.01 * w.N)
+        for b in range(w.B):
+            for hk in range(w.H_kv):
+                rows = torch.randperm(w.N, generator=g, device=device)[:n_rows]
+                k[b, hk, rows] = k[b, hk, rows] * 8
+    return Inputs(q.contiguous(), k.contiguous(), v.contiguous(), kv_len, w.scale, w.causal)
+
+
+def effective_flops(w: Workload, kv_len=None) -> float:
+    """4 d per unmasked (query, key) pair, summed over batches and heads: the work the masks leave
+    (kv_len given as a host sequence of B lengths, or None)."""
+    total = 0
+    for b in range(w.B):
+        L = w.N if kv_len is None else min(max(int(kv_len[b]), 0), w.N)
+        if w.causal:  # row i sees min(L, i + 1) keys
+            total += L * (L + 1) // 2 + (w.N - L) * L
+        else:
+            total += w.N * L
+    return 4.0 * w.d * w.H * total
+
+
 def custom(B: int, H: int, H_kv: int, N: int, d: int, dtype: str = "bf16", *, causal: bool = False,
            padded: bool = False, peaky: bool = False, seed: int = 0, kv_len=None) -> Inputs:
     """Inputs of an arbitrary shape (edge-case tests); ``kv_len`` overrides the drawn lengths."""

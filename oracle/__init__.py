@@ -7,7 +7,8 @@ the CUDA path; the two meet only in the seeded inputs of ``exact_tiled_attention
 ``attn_oracle.c`` is the plain definition (full N x N score matrix per head, fp64) plus a row-sampled
 evaluator of the same definition and a tiled restatement of the online-softmax recurrence;
 ``attn_oracle_np.py`` is an independent NumPy restatement for small cases, the merge of results over
-disjoint key sets (split-KV), and the backward pass (dQ, dK, dV) of the same attention.
+disjoint key sets (split-KV), and the backward pass (dQ, dK, dV) of the same attention, whole or at
+selected rows and keys (for sequences too long for the whole matrices).
 """
 from __future__ import annotations
 
@@ -48,6 +49,8 @@ def _load():
         for fn in (lib.oracle_attn_f64, lib.oracle_attn_rows_f64, lib.oracle_attn_tiled_f64):
             fn.restype = ci
         lib.oracle_num_threads.restype = ci
+        lib.oracle_set_num_threads.argtypes = [ci]
+        lib.oracle_set_num_threads.restype = None
         _lib = lib
     return _lib
 
@@ -75,6 +78,11 @@ def _lens(kv_len, B):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the following C-oracle calls (all host cores by default)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def attention(q, k, v, scale, causal=False, kv_len=None, return_p=False):
@@ -135,6 +143,7 @@ def attention_tiled(q, k, v, scale, causal=False, kv_len=None, Br=16, Bc=16):
     return O, LSE
 
 
-from .attn_oracle_np import (attention_bias_dropout_np, attention_bwd_np, attention_fp8_np,  # noqa: E402
+from .attn_oracle_np import (attention_bias_dropout_np, attention_bwd_np, attention_bwd_sampled_np,  # noqa: E402
+                             attention_fp8_np,
                              attention_np, dropout_keep_mask, dropout_threshold, e4m3_round, fwht_f32, merge_np,
                              philox4x32_10, quantize_e4m3_tiles, tile_exponent)

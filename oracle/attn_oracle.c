@@ -63,6 +63,15 @@ static int clamp_len(const int32_t* kv_len, int b, int N) {
     return L;
 }
 
+/* Threads the following calls use (benchmark legs time the oracle on one core as well as on all). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -123,6 +123,84 @@ def attention_bwd_np(q, k, v, dO, scale, causal=False, kv_len=None):
     return dQ, dK, dV
 
 
+def _head_stats_np(qh, kh, vh, scale, mask, block=512):
+    """O [N, d] and LSE [N] of one head, exact in fp64, computed over blocks of query rows (the same
+    definition as attention_np, without holding the N x N matrix at once)."""
+    N, d = qh.shape
+    O = np.zeros((N, d))
+    LSE = np.full(N, -np.inf)
+    for r0 in range(0, N, block):
+        r1 = min(N, r0 + block)
+        S = float(scale) * (qh[r0:r1] @ kh.T)
+        S = np.where(mask[r0:r1], S, -np.inf)
+        m = S.max(axis=1)
+        has = np.isfinite(m)
+        m_safe = np.where(has, m, 0.0)
+        E = np.exp(S - m_safe[:, None])
+        l = E.sum(axis=1)
+        O[r0:r1] = np.where(has[:, None], (E @ vh) / np.where(has, l, 1.0)[:, None], 0.0)
+        with np.errstate(divide="ignore"):
+            LSE[r0:r1] = np.where(has, m_safe + np.log(np.where(has, l, 1.0)), -np.inf)
+    return O, LSE
+
+
+def attention_bwd_sampled_np(q, k, v, dO, scale, b, h, rows, keys, causal=False, kv_len=None):
+    """The gradients of attention_bwd_np at selected positions, exact in fp64, for sequences too long
+    for the whole N x N matrices: dQ[b, h, rows] of query head h, and dK[b, kh, keys], dV[b, kh, keys]
+    of the key/value head kh = h / (H / H_kv) that head reads (summed over every query head of its
+    group, as in attention_bwd_np). Each entry is the same chain rule, evaluated over all N keys or
+    all N query rows:
+        P_ij = exp(S_ij - LSE_i) (0 where masked),  D_i = sum_c dO_ic O_ic,
+        dS_ij = P_ij (dO_i . V_j - D_i),
+        dQ_i = scale sum_j dS_ij K_j,  dK_j = scale sum_i dS_ij Q_i,  dV_j = sum_i P_ij dO_i,
+    with O and LSE of every query row from the exact forward (computed in blocks of rows).
+    Returns a dict with dq [len(rows), d], dk and dv [len(keys), d], and O [g, N, d], LSE [g, N] of
+    the group's query heads (h's own at index h mod g), P_rows [len(rows), N] and P_keys
+    [g, N, len(keys)] (the probabilities used) and dS_rows / dS_keys likewise.
+    """
+    q = np.asarray(q)
+    k = np.asarray(k)
+    v = np.asarray(v)
+    dO = np.asarray(dO)
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    g = H // H_kv
+    kh = h // g
+    rows = np.asarray(rows, dtype=np.int64)
+    keys = np.asarray(keys, dtype=np.int64)
+    L = N if kv_len is None else int(kv_len[b])
+    mask = key_mask(N, causal, L)
+    K = np.asarray(k[b, kh], dtype=np.float64)
+    V = np.asarray(v[b, kh], dtype=np.float64)
+    out = dict(dk=np.zeros((len(keys), d)), dv=np.zeros((len(keys), d)), O=np.zeros((g, N, d)),
+               LSE=np.zeros((g, N)), P_keys=np.zeros((g, N, len(keys))), dS_keys=np.zeros((g, N, len(keys))))
+    for t in range(g):
+        hq = kh * g + t
+        Q = np.asarray(q[b, hq], dtype=np.float64)
+        G = np.asarray(dO[b, hq], dtype=np.float64)
+        O, LSE = _head_stats_np(Q, K, V, scale, mask)
+        D = np.sum(G * O, axis=1)
+        has = np.isfinite(LSE)
+        lse_safe = np.where(has, LSE, 0.0)
+        out["O"][t], out["LSE"][t] = O, LSE
+        # columns `keys` of P and dS over every query row
+        Sk = float(scale) * (Q @ K[keys].T)
+        Pk = np.where(mask[:, keys] & has[:, None], np.exp(np.where(mask[:, keys], Sk, 0.0) - lse_safe[:, None]), 0.0)
+        dSk = Pk * (G @ V[keys].T - D[:, None])
+        out["dv"] += Pk.T @ G
+        out["dk"] += float(scale) * (dSk.T @ Q)
+        out["P_keys"][t], out["dS_keys"][t] = Pk, dSk
+        if hq == h:
+            # rows `rows` of P and dS over every key
+            Sr = float(scale) * (Q[rows] @ K.T)
+            mr = mask[rows] & has[rows][:, None]
+            Pr = np.where(mr, np.exp(np.where(mask[rows], Sr, 0.0) - lse_safe[rows][:, None]), 0.0)
+            dSr = Pr * (G[rows] @ V.T - D[rows][:, None])
+            out["dq"] = float(scale) * (dSr @ K)
+            out["P_rows"], out["dS_rows"] = Pr, dSr
+    return out
+
+
 # ------------------------------------------------------------------------------------------------
 # fp8 forward with incoherent processing (section "闪电注意力-3" of "闪电注意力：革命性地提高Transformer
 # 效率", unite.ai: FP8 computation, and a processing step that lowers the quantisation error of the

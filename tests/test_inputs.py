@@ -36,3 +36,18 @@ def test_headline_workload():
     w = inputs.WORKLOADS[inputs.HEADLINE]
     assert (w.B, w.H, w.N, w.d, w.causal) == (1, 16, 8192, 128, False)
     assert w.nominal_flops() == 4 * 16 * 8192 ** 2 * 128
+
+
+def test_effective_flops_counts_the_unmasked_pairs():
+    """4 d per (query, key) pair the masks leave, against a brute-force count."""
+    import numpy as np
+    for causal in (False, True):
+        for lens in (None, [5, 13, 0]):
+            w = inputs.Workload("t", 3, 2, 1, 13, 64, "bf16", causal=causal, padded=lens is not None)
+            count = 0
+            for b in range(3):
+                L = 13 if lens is None else lens[b]
+                i, j = np.meshgrid(np.arange(13), np.arange(13), indexing="ij")
+                ok = (j < L) & ((j <= i) if causal else True)
+                count += int(ok.sum()) * 2  # two heads
+            assert inputs.effective_flops(w, lens) == 4.0 * 64 * count

@@ -111,3 +111,70 @@ def test_planted_backward_mistake_is_caught(name):
     ours = ns["attention_bwd_np"](q, k, v, dO, 0.45, causal=True, kv_len=[5, 9])
     ref = _torch_grads(q, k, v, dO, 0.45, True, [5, 9])
     assert any(not np.allclose(a, b, rtol=0, atol=1e-9) for a, b in zip(ours, ref))
+
+
+# ---------------------------------------------------------------- the row/key-sampled backward oracle
+SAMPLED_CASES = [
+    dict(causal=False, kv_len=None, H_kv=4),
+    dict(causal=True, kv_len=None, H_kv=2),
+    dict(causal=False, kv_len=[37, 0], H_kv=1),
+    dict(causal=True, kv_len=[50, 23], H_kv=4),
+]
+
+
+@pytest.mark.parametrize("case", SAMPLED_CASES)
+def test_sampled_backward_equals_torch_autograd(case):
+    """Every sampled entry equals torch's fp64 autograd of the explicit masked softmax (a library
+    routine), over sizes that span several blocks of the forward pass (N = 1100 > its 512-row blocks)."""
+    rng = np.random.default_rng(5)
+    B, H, N, d = 2, 4, 1100, 8
+    q, k, v, dO = _inputs(11, B=B, H=H, H_kv=case["H_kv"], N=N, d=d)
+    scale = 0.37
+    tq, tk, tv = _torch_grads(q, k, v, dO, scale, case["causal"], case["kv_len"])
+    g = H // case["H_kv"]
+    for b, h in [(0, 1), (1, H - 1)]:
+        rows = np.sort(rng.choice(N, size=17, replace=False))
+        keys = np.sort(rng.choice(N, size=13, replace=False))
+        r = oracle.attention_bwd_sampled_np(q, k, v, dO, scale, b, h, rows, keys, causal=case["causal"],
+                                            kv_len=case["kv_len"])
+        np.testing.assert_allclose(r["dq"], tq[b, h, rows], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(r["dk"], tk[b, h // g, keys], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(r["dv"], tv[b, h // g, keys], rtol=0, atol=1e-12)
+
+
+def test_sampled_backward_equals_the_whole_backward():
+    q, k, v, dO = _inputs(12, B=1, H=4, H_kv=2, N=300, d=16)
+    full = oracle.attention_bwd_np(q, k, v, dO, 0.25, causal=True, kv_len=[290])
+    O, L = oracle.attention_np(q, k, v, 0.25, causal=True, kv_len=[290])
+    rows, keys = np.arange(0, 300, 7), np.arange(3, 300, 11)
+    r = oracle.attention_bwd_sampled_np(q, k, v, dO, 0.25, 0, 3, rows, keys, causal=True, kv_len=[290])
+    np.testing.assert_allclose(r["dq"], full[0][0, 3, rows], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["dk"], full[1][0, 1, keys], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["dv"], full[2][0, 1, keys], rtol=0, atol=1e-12)
+    # the forward statistics it returns are the forward oracle's (query heads 2 and 3 read kv head 1)
+    np.testing.assert_allclose(r["O"], O[0, 2:4], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["LSE"][np.isfinite(r["LSE"])], L[0, 2:4][np.isfinite(L[0, 2:4])], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("mutant", ["D_dropped", "dK_without_group_sum", "dV_from_dS"])
+def test_sampled_backward_planted_mistakes_fail_the_pin(mutant, monkeypatch):
+    """Mistakes planted in a copy of the sampled oracle (the D term dropped, a grouped key/value head
+    taking one query head only, dV from dS instead of P) each break agreement with torch autograd."""
+    import oracle.attn_oracle_np as onp
+    src = __import__("inspect").getsource(onp.attention_bwd_sampled_np)
+    plant = {
+        "D_dropped": ("dSk = Pk * (G @ V[keys].T - D[:, None])", "dSk = Pk * (G @ V[keys].T)"),
+        "dK_without_group_sum": ('out["dk"] += float(scale) * (dSk.T @ Q)',
+                                 'out["dk"] = float(scale) * (dSk.T @ Q) if t == 0 else out["dk"]'),
+        "dV_from_dS": ('out["dv"] += Pk.T @ G', 'out["dv"] += dSk.T @ G'),
+    }[mutant]
+    assert plant[0] in src
+    ns = dict(vars(onp))
+    exec(src.replace(plant[0], plant[1]), ns)
+    q, k, v, dO = _inputs(13, B=1, H=4, H_kv=2, N=40, d=6)
+    tq, tk, tv = _torch_grads(q, k, v, dO, 0.5, False, None)
+    keys = np.arange(40)
+    r = ns["attention_bwd_sampled_np"](q, k, v, dO, 0.5, 0, 1, np.arange(40), keys)
+    ok = (np.allclose(r["dq"], tq[0, 1], atol=1e-9) and np.allclose(r["dk"], tk[0, 0], atol=1e-9)
+          and np.allclose(r["dv"], tv[0, 0], atol=1e-9))
+    assert not ok
