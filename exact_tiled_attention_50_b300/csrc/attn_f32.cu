@@ -10,7 +10,7 @@
 // Mapping: a CTA of 256 threads (8 warps) owns 8 query rows of one (b, h) and splits the key range
 // into 8 slices, one per warp, so that short sequences still spread over many warps: in a warp, four
 // consecutive lanes share a row and each holds a quarter of its query and output columns. Every warp
-// runs the online softmax over its slice (keys read straight from L2, 8 at a time); the 8 partial
+// runs the online softmax over its slice (key rows read straight from L2, 8 or 4 at a time); the 8 partial
 // results of a row are then combined in shared memory with the softmax merge rule (formula 2 of
 // "闪电注意力的数学原理" on the unite.ai page: m = max m_w, l = sum l_w e^(m_w - m), O = sum O_w
 // e^(m_w - m) / l).
@@ -26,12 +26,12 @@ namespace {
 constexpr int F32_ROWS = 8;      // query rows per CTA
 constexpr int F32_WARPS = 8;     // key slices per CTA
 constexpr int F32_THREADS = 32 * F32_WARPS;
-constexpr int F32_CHUNK = 8;     // keys per online-softmax update
 }  // namespace
 
 template <int D>
 __global__ void __launch_bounds__(F32_THREADS) attn_fwd_f32_kernel(const F32Params p) {
-    constexpr int CPL = D / 4;  // columns per lane
+    constexpr int CPL = D / 4;            // columns per lane
+    constexpr int CH = D == 64 ? 8 : 4;   // keys per online-softmax update (their rows held in registers)
     __shared__ __align__(16) float sm_o[F32_WARPS][F32_ROWS][D];
     __shared__ float sm_m[F32_WARPS][F32_ROWS], sm_l[F32_WARPS][F32_ROWS];
     __shared__ float sm_w[F32_WARPS][F32_ROWS], sm_inv[F32_ROWS], sm_lse[F32_ROWS];
@@ -74,30 +74,42 @@ __global__ void __launch_bounds__(F32_THREADS) attn_fwd_f32_kernel(const F32Para
     for (int i = 0; i < CPL; ++i) o[i] = 0.f;
     float m = -INFINITY, l = 0.f;
 
-    for (int k0 = k_begin; k0 < k_end; k0 += F32_CHUNK) {  // warp-uniform loop
-        float s[F32_CHUNK];
+    for (int k0 = k_begin; k0 < k_end; k0 += CH) {  // warp-uniform loop
+        // every key row of the chunk is requested before any is used, so that the chunk costs one
+        // memory latency for K and one for V (issued while the exponentials run)
+        float4 kv[CH][CPL / 4];
 #pragma unroll
-        for (int j = 0; j < F32_CHUNK; ++j) {
-            const int key = k0 + j;
+        for (int j = 0; j < CH; ++j) {
+            const float4* k4 = reinterpret_cast<const float4*>(Kp + static_cast<size_t>(k0 + j) * D);
+#pragma unroll
+            for (int i = 0; i < CPL / 4; ++i)
+                kv[j][i] = (k0 + j < k_end) ? __ldg(k4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float s[CH];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
             float acc = 0.f;
-            if (key < k_end) {
-                const float4* k4 = reinterpret_cast<const float4*>(Kp + static_cast<size_t>(key) * D);
 #pragma unroll
-                for (int i = 0; i < CPL / 4; ++i) {
-                    const float4 kv = __ldg(k4 + i);
-                    acc = fmaf(q[4 * i], kv.x, acc);
-                    acc = fmaf(q[4 * i + 1], kv.y, acc);
-                    acc = fmaf(q[4 * i + 2], kv.z, acc);
-                    acc = fmaf(q[4 * i + 3], kv.w, acc);
-                }
+            for (int i = 0; i < CPL / 4; ++i) {
+                acc = fmaf(q[4 * i], kv[j][i].x, acc);
+                acc = fmaf(q[4 * i + 1], kv[j][i].y, acc);
+                acc = fmaf(q[4 * i + 2], kv[j][i].z, acc);
+                acc = fmaf(q[4 * i + 3], kv[j][i].w, acc);
             }
             acc += __shfl_xor_sync(0xffffffffu, acc, 1);
             acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            s[j] = (key < k_end && key < row_lim) ? acc * p.scale : -INFINITY;
+            s[j] = (k0 + j < k_end && k0 + j < row_lim) ? acc * p.scale : -INFINITY;
+        }
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {  // V rows of the chunk into the registers K used
+            const float4* v4 = reinterpret_cast<const float4*>(Vp + static_cast<size_t>(k0 + j) * D);
+#pragma unroll
+            for (int i = 0; i < CPL / 4; ++i)
+                kv[j][i] = (k0 + j < k_end) ? __ldg(v4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float mt = s[0];
 #pragma unroll
-        for (int j = 1; j < F32_CHUNK; ++j) mt = fmaxf(mt, s[j]);
+        for (int j = 1; j < CH; ++j) mt = fmaxf(mt, s[j]);
         const float m_new = fmaxf(m, mt);
         // no valid key yet: m_new = -inf, every probability is 0 and o, l stay 0
         const float alpha = (m == -INFINITY) ? 0.f : expf(m - m_new);
@@ -105,19 +117,15 @@ __global__ void __launch_bounds__(F32_THREADS) attn_fwd_f32_kernel(const F32Para
 #pragma unroll
         for (int i = 0; i < CPL; ++i) o[i] *= alpha;
 #pragma unroll
-        for (int j = 0; j < F32_CHUNK; ++j) {
+        for (int j = 0; j < CH; ++j) {
             const float pj = (s[j] == -INFINITY) ? 0.f : expf(s[j] - m_new);
             l += pj;
-            if (k0 + j < k_end) {
-                const float4* v4 = reinterpret_cast<const float4*>(Vp + static_cast<size_t>(k0 + j) * D);
 #pragma unroll
-                for (int i = 0; i < CPL / 4; ++i) {
-                    const float4 vv = __ldg(v4 + i);
-                    o[4 * i] = fmaf(pj, vv.x, o[4 * i]);
-                    o[4 * i + 1] = fmaf(pj, vv.y, o[4 * i + 1]);
-                    o[4 * i + 2] = fmaf(pj, vv.z, o[4 * i + 2]);
-                    o[4 * i + 3] = fmaf(pj, vv.w, o[4 * i + 3]);
-                }
+            for (int i = 0; i < CPL / 4; ++i) {
+                o[4 * i] = fmaf(pj, kv[j][i].x, o[4 * i]);
+                o[4 * i + 1] = fmaf(pj, kv[j][i].y, o[4 * i + 1]);
+                o[4 * i + 2] = fmaf(pj, kv[j][i].z, o[4 * i + 2]);
+                o[4 * i + 3] = fmaf(pj, kv[j][i].w, o[4 * i + 3]);
             }
         }
         m = m_new;

@@ -137,12 +137,14 @@ template <class Tab>
 __host__ __device__ inline bool walk_next(WalkState& w, const Tab& t, const SchedPlan& p, int cta, Segment& s) {
     const long long u_dp = static_cast<long long>(w.round) * p.G + cta;
     if (w.round < p.R_dp && u_dp < p.units) {
-        const long long u = u_dp;
+        // 32-bit arithmetic: units < 2^31 (every unit costs at least one step of a line below 2^31)
+        const unsigned u = static_cast<unsigned>(u_dp);
         ++w.round;
-        const long long per_b = static_cast<long long>(p.H) * p.n_pairs;
-        s.b = static_cast<int>(u / per_b);
-        s.h = static_cast<int>((u / p.n_pairs) % p.H);
-        s.pair = static_cast<int>(u % p.n_pairs);
+        const unsigned np = static_cast<unsigned>(p.n_pairs);
+        const unsigned bh = u / np;
+        s.pair = static_cast<int>(u - bh * np);
+        s.b = static_cast<int>(bh / static_cast<unsigned>(p.H));
+        s.h = static_cast<int>(bh - static_cast<unsigned>(s.b) * static_cast<unsigned>(p.H));
         const int nb = t.nb(s.b);
         s.cost = pair_cost(s.pair, nb, p.N, p.causal);
         s.k0 = 0;

@@ -150,6 +150,10 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1
     return x;
 }
 
+// 2^k as fp32 for the exponents the merge and epilogue use (k <= 127; 0 below 2^-126, where the
+// weighted contribution is negligible)
+__device__ __forceinline__ float pow2i(int k) { return k < -126 ? 0.f : __int_as_float((k + 127) << 23); }
+
 __device__ __forceinline__ int clamp_len(const int32_t* kv_len, int b, int N) {
     if (!kv_len) return N;
     int L = __ldg(kv_len + b);
@@ -925,11 +929,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (t == 0 && r == 0) ATTN_SEG_TRACE(seg_no, 8, static_cast<long long>(global_timer_ns()));
             // softmax merge of the pieces: weights 2^(m_i - M) on l, 2^(m_i - M + E_i - Emax) on O
             const float w_own_l = live ? ex2_approx(m_run - M) : 0.f;
-            const float w_own = live ? ldexpf(w_own_l, E - Emax) : 0.f;
+            const float w_own = live ? w_own_l * pow2i(E - Emax) : 0.f;
             const float w0l = pl0 > 0.f ? ex2_approx(pm0 - M) : 0.f;
             const float w1l = pl1 > 0.f ? ex2_approx(pm1 - M) : 0.f;
-            const float w0 = pl0 > 0.f ? ldexpf(w0l, pe0 - Emax) : 0.f;
-            const float w1 = pl1 > 0.f ? ldexpf(w1l, pe1 - Emax) : 0.f;
+            const float w0 = pl0 > 0.f ? w0l * pow2i(pe0 - Emax) : 0.f;
+            const float w1 = pl1 > 0.f ? w1l * pow2i(pe1 - Emax) : 0.f;
             float L = w_own_l * l_run + w0l * pl0 + w1l * pl1;
             int c_extra = c_end;  // first CTA whose piece is beyond the two kept in registers
             if (np > 2) {
@@ -950,13 +954,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (t == 0 && r == 0) ATTN_SEG_TRACE(seg_no, 9, static_cast<long long>(global_timer_ns()));
             const int bh = s.b * p.plan.H + s.h;
-            float inv = L > 0.f ? ldexpf(1.0f, Emax) / L : 0.f;
+            float inv = L > 0.f ? pow2i(Emax) * __frcp_rn(L) : 0.f;
             if constexpr (EXTRA) inv *= p.keep_scale;  // inverted dropout (1 without dropout)
             const bool store = row < p.plan.N;
             const size_t obase = (static_cast<size_t>(bh) * p.plan.N + (store ? row : 0)) * D;
             const uint32_t stage_base = smem_u32(smem + t * C::TILE_BYTES + wq * C::EPI_BUFS * 4096);
+            // A unit with no other pieces (the usual case) and fp32 output: two chunks per pass, both
+            // read from tensor memory together and staged behind one proxy fence; the weight and the
+            // normalisation fold into one factor.
+            const bool fast = !OUT_BF16 && C::EPI_BUFS >= 2 && np == 0 && seg_loads_q;
+            if (fast) {
+                const float sc = have ? w_own * inv : 0.f;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 32; c += 2) {
+                    uint32_t oa[32], ob[32];
+                    if (have) {
+                        tmem_ld32(tO + c * 32, oa);
+                        tmem_ld32(tO + (c + 1) * 32, ob);
+                        tmem_wait_ld(oa);
+                        tmem_wait_ld(ob);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) oa[i] = ob[i] = 0u;
+                    }
+                    if (c >= C::EPI_BUFS) {  // the store engine has read the buffers of the last pass
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+                    }
+                    const uint32_t bufa = stage_base + (c % C::EPI_BUFS) * 4096;
+                    const uint32_t bufb = stage_base + ((c + 1) % C::EPI_BUFS) * 4096;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t off = lane * 128 + ((k ^ (lane & 7)) << 4);
+                        st_shared_v4(bufa + off, __float_as_uint(__uint_as_float(oa[4 * k]) * sc),
+                                     __float_as_uint(__uint_as_float(oa[4 * k + 1]) * sc),
+                                     __float_as_uint(__uint_as_float(oa[4 * k + 2]) * sc),
+                                     __float_as_uint(__uint_as_float(oa[4 * k + 3]) * sc));
+                        st_shared_v4(bufb + off, __float_as_uint(__uint_as_float(ob[4 * k]) * sc),
+                                     __float_as_uint(__uint_as_float(ob[4 * k + 1]) * sc),
+                                     __float_as_uint(__uint_as_float(ob[4 * k + 2]) * sc),
+                                     __float_as_uint(__uint_as_float(ob[4 * k + 3]) * sc));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tmO, smem + (bufa - smem_u32(smem)), c * 32, q0t + wq * 32, bh);
+                        tma_store_3d(&tmO, smem + (bufb - smem_u32(smem)), (c + 1) * 32, q0t + wq * 32, bh);
+                        bulk_commit_group();
+                    }
+                    __syncwarp();
+                }
+            }
+#pragma unroll 1
+            for (int c = 0; c < (fast ? 0 : D / 32); ++c) {
                 uint32_t o[32];
                 if (have) {
                     tmem_ld32(tO + c * 32, o);
