@@ -260,6 +260,10 @@ attn_status run_bf16_path(const void* Q, const void* K, const void* V, void* O, 
         p.drop_t = ex->drop_t;
         p.seed_lo = ex->seed_lo;
         p.seed_hi = ex->seed_hi;
+        for (int r = 0; r < 10; ++r) {  // Philox4x32-10 key schedule: Weyl increments W0, W1 per round
+            p.round_key[0][r] = ex->seed_lo + static_cast<uint32_t>(r) * 0x9E3779B9u;
+            p.round_key[1][r] = ex->seed_hi + static_cast<uint32_t>(r) * 0xBB67AE85u;
+        }
         p.rng_offset = ex->rng_offset;
         p.keep_scale = ex->keep_scale;
     }

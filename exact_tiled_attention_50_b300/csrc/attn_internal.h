@@ -218,6 +218,9 @@ struct TcParams {
     const uint16_t* bias;
     long long bias_sb, bias_sh, bias_sr;
     uint32_t drop_t, seed_lo, seed_hi, rng_offset;
+    // the generator's ten round keys (k0 + r W0, k1 + r W1 for r = 0..9), the same for every draw of a
+    // launch: computed once on the host, read by the kernel from its parameter space
+    uint32_t round_key[2][10];
     float keep_scale;
 };
 

@@ -137,15 +137,15 @@ __device__ __forceinline__ void record_failure(volatile int* abort_flag, uint32_
 
 // Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2,
 // 3", SC 2011): per round the 64-bit products M0 * x0 and M1 * x2 are split into halves and
-// x <- (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0); the key then advances by (W0, W1).
-__device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
+// x <- (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0), the key of round r being (k0 + r W0, k1 + r W1).
+// The round keys are the same for every draw of a launch and come precomputed (rk[0][r], rk[1][r]).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, const uint32_t (&rk)[2][10]) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t hi0 = __umulhi(0xD2511F53u, x.x), lo0 = 0xD2511F53u * x.x;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, x.z), lo1 = 0xCD9E8D57u * x.z;
-        x = make_uint4(hi1 ^ x.y ^ k0, lo1, hi0 ^ x.w ^ k1, lo0);
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
+        const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * x.x;
+        const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * x.z;
+        x = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ x.y ^ rk[0][r], static_cast<uint32_t>(p1),
+                       static_cast<uint32_t>(p0 >> 32) ^ x.w ^ rk[1][r], static_cast<uint32_t>(p0));
     }
     return x;
 }
@@ -813,7 +813,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                 make_uint4(static_cast<uint32_t>((key0 + 64 * half + 2 * i) >> 3),
                                                            static_cast<uint32_t>(row),
                                                            static_cast<uint32_t>(s.b * p.plan.H + s.h), p.rng_offset),
-                                                p.seed_lo, p.seed_hi);
+                                                p.round_key);
                                         const uint32_t w = (i & 3) == 0 ? rnd.x : (i & 3) == 1 ? rnd.y
                                                          : (i & 3) == 2 ? rnd.z : rnd.w;
                                         if ((w & 0xffffu) < p.drop_t) e0 = 0.f;
@@ -1121,14 +1121,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 __device__ void plan_block(const PlanParams& pl) {
     __shared__ long long part[256];
     const int tid = threadIdx.x;
+    const bool act = tid < 256;  // 256 partial sums; larger blocks' other threads only clear flags
     const int per = (pl.B + 255) / 256;
-    const int b0 = min(pl.B, tid * per), b1 = min(pl.B, b0 + per);
+    const int b0 = act ? min(pl.B, tid * per) : 0, b1 = act ? min(pl.B, b0 + per) : 0;
     long long sum = 0;
     for (int b = b0; b < b1; ++b) {
         const int nb = key_tiles(clamp_len(pl.kv_len, b, pl.N));
         sum += static_cast<long long>(pl.H) * pair_prefix(pl.n_pairs, nb, pl.N, pl.causal);
     }
-    part[tid] = sum;
+    if (act) part[tid] = sum;
     __syncthreads();
     if (tid == 0) {  // exclusive scan of 256 partial sums
         long long run = 0;
@@ -1140,13 +1141,13 @@ __device__ void plan_block(const PlanParams& pl) {
         pl.boff[pl.B] = run;
     }
     __syncthreads();
-    long long run = part[tid];
+    long long run = act ? part[tid] : 0;
     for (int b = b0; b < b1; ++b) {
         pl.boff[b] = run;
         const int nb = key_tiles(clamp_len(pl.kv_len, b, pl.N));
         run += static_cast<long long>(pl.H) * pair_prefix(pl.n_pairs, nb, pl.N, pl.causal);
     }
-    for (int i = tid; i < 8 * SCHED_MAX_CTAS; i += 256) pl.flags[i] = 0u;
+    for (int i = tid; i < 8 * SCHED_MAX_CTAS; i += blockDim.x) pl.flags[i] = 0u;
 }
 
 constexpr int VPREP_THREADS = 256;
@@ -1211,12 +1212,13 @@ cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStrea
 }
 
 // ---------------------------------------------------------------------------------------------
-// fp8 pre-pass (d = 128): one block per 128-row tile of Q, K or V, plus the plan block.
+// fp8 pre-pass (d = 128): one block of 512 threads per 128-row tile of Q, K or V, plus the plan block.
 // Q and K rows are multiplied by the signs and transformed by the unnormalised Walsh-Hadamard
 // butterflies (spans 1, 2, 4, ..., 64 in that order; each output one fp32 addition or subtraction),
-// then every tile is rounded to E4M3 at its own power-of-two scale.
+// then every tile is rounded to E4M3 at its own power-of-two scale. Four threads share a row (32
+// elements each), so that a thread needs few registers and many tiles stream through an SM at once.
 // ---------------------------------------------------------------------------------------------
-constexpr int FP8P_THREADS = 256;
+constexpr int FP8P_THREADS = 512;
 
 // Tile exponent from the largest |x| as fp32 bits: max |x| < 2^(e8 - 126); e = max(e8 - 134, -100)
 // keeps the tile's values times 2^-e below 256 = 2^8 (E4M3 holds up to 448); a zero tile gets 0.
@@ -1240,17 +1242,18 @@ __device__ __forceinline__ uint32_t fp8_block_max(uint32_t v, uint32_t* red) {
 // 2^-e as fp32 for e in [-100, 120]
 __device__ __forceinline__ float fp8_pow2_neg(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
 
-// One 128-row tile of Q or K: thread t holds row t / 2, elements 64 (t mod 2) .. +63. Butterflies
-// of spans 1 .. 32 run inside the thread, span 64 pairs the two threads of a row (lanes 2r, 2r+1).
+// One 128-row tile of Q or K: thread t holds row t / 4, elements 32 (t mod 4) .. +31. Butterflies of
+// spans 1 .. 16 run inside the thread, span 32 pairs lanes 4r + q and 4r + (q ^ 1), span 64 lanes
+// 4r + q and 4r + (q ^ 2); the lower element of a pair keeps x + y, the upper x - y.
 __device__ void fp8_prep_qk_tile(const __nv_bfloat16* src, uint8_t* dst, int32_t* exp_out, const int8_t* signs,
                                  int N, int tile, uint32_t* red) {
-    const int half = threadIdx.x & 1;
-    const int row = tile * 128 + (threadIdx.x >> 1);
-    float a[64];
+    const int q4 = threadIdx.x & 3;
+    const int row = tile * 128 + (threadIdx.x >> 2);
+    float a[32];
     if (row < N) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * 128 + half * 64);
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * 128 + q4 * 32);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
             const uint4 u = __ldg(s4 + k);
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -1261,15 +1264,15 @@ __device__ void fp8_prep_qk_tile(const __nv_bfloat16* src, uint8_t* dst, int32_t
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) a[i] = 0.f;
+        for (int i = 0; i < 32; ++i) a[i] = 0.f;
     }
     if (signs) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) a[i] *= static_cast<float>(__ldg(signs + half * 64 + i));
+        for (int i = 0; i < 32; ++i) a[i] *= static_cast<float>(__ldg(signs + q4 * 32 + i));
 #pragma unroll
-        for (int h = 1; h < 64; h <<= 1) {
+        for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
+            for (int i = 0; i < 32; ++i) {
                 if (i & h) continue;
                 const float x = a[i], y = a[i + h];
                 a[i] = x + y;
@@ -1277,21 +1280,26 @@ __device__ void fp8_prep_qk_tile(const __nv_bfloat16* src, uint8_t* dst, int32_t
             }
         }
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {  // span 64: the lower half keeps x + y, the upper x - y
+        for (int i = 0; i < 32; ++i) {  // span 32
             const float o = __shfl_xor_sync(0xffffffffu, a[i], 1);
-            a[i] = half ? o - a[i] : a[i] + o;
+            a[i] = (q4 & 1) ? o - a[i] : a[i] + o;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {  // span 64
+            const float o = __shfl_xor_sync(0xffffffffu, a[i], 2);
+            a[i] = (q4 & 2) ? o - a[i] : a[i] + o;
         }
     }
     uint32_t mbits = 0;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) mbits = max(mbits, __float_as_uint(a[i]) & 0x7fffffffu);
+    for (int i = 0; i < 32; ++i) mbits = max(mbits, __float_as_uint(a[i]) & 0x7fffffffu);
     const int e = fp8_tile_exponent(fp8_block_max(mbits, red));
     if (threadIdx.x == 0) *exp_out = e;
     const float sc = fp8_pow2_neg(e);
     if (row < N) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * 128 + half * 64);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * 128 + q4 * 32);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 2; ++k) {
             uint32_t w[4];
 #pragma unroll
             for (int e4 = 0; e4 < 4; ++e4) {
@@ -1304,14 +1312,16 @@ __device__ void fp8_prep_qk_tile(const __nv_bfloat16* src, uint8_t* dst, int32_t
 }
 
 // One 128-key tile of V, rounded and written transposed: dst row c (dimension c) holds the tile's
-// 128 keys at columns tile*128 ..; keys past N are zero.
+// 128 keys at columns tile*128 ..; keys past N are zero. The tile passes through shared memory with
+// its columns XOR-swizzled by the key's 32-row group, so that the transposed reads of a warp (8
+// dimensions x 4 key groups) fall in distinct banks.
 __device__ void fp8_prep_v_tile(const __nv_bfloat16* src, uint8_t* dstT, int32_t* exp_out, int N, int n_cols,
                                 int tile, uint32_t* red, uint16_t (*sm)[130]) {
     uint32_t mbits = 0;  // largest |V| as bf16 bits
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 4; ++k) {
         const int idx = threadIdx.x + k * FP8P_THREADS;  // 16-byte vector of the tile: row idx/16
-        const int row = idx >> 4, c8 = (idx & 15) * 8;
+        const int row = idx >> 4, c8 = ((idx & 15) * 8) ^ ((row >> 5) << 3);
         uint4 u = make_uint4(0u, 0u, 0u, 0u);
         if (tile * 128 + row < N)
             u = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(tile * 128 + row) * 128) + (idx & 15));
@@ -1326,18 +1336,19 @@ __device__ void fp8_prep_v_tile(const __nv_bfloat16* src, uint8_t* dstT, int32_t
     const int e = fp8_tile_exponent(fp8_block_max(mbits << 16, red));  // (the reduction synchronises sm)
     if (threadIdx.x == 0) *exp_out = e;
     const float sc = fp8_pow2_neg(e);
-    const int c = threadIdx.x >> 1, k0 = (threadIdx.x & 1) * 64;
-    uint32_t o[16];
+    const int c = threadIdx.x >> 2, kg = threadIdx.x & 3, k0 = kg * 32;  // dimension c, keys k0 .. k0 + 31
+    const int cs = c ^ (kg << 3);                                          // its swizzled column
+    uint32_t o[8];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
+    for (int q = 0; q < 8; ++q) {
         float f[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) f[u] = __uint_as_float(static_cast<uint32_t>(sm[k0 + 4 * q + u][c]) << 16) * sc;
+        for (int u = 0; u < 4; ++u) f[u] = __uint_as_float(static_cast<uint32_t>(sm[k0 + 4 * q + u][cs]) << 16) * sc;
         o[q] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
     }
     uint4* dst = reinterpret_cast<uint4*>(dstT + static_cast<size_t>(c) * n_cols + tile * 128 + k0);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 __global__ void __launch_bounds__(FP8P_THREADS) fp8_prep_kernel(const Fp8PrepParams p, const PlanParams pl) {
