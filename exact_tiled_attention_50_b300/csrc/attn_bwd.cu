@@ -88,8 +88,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int jt = blockIdx.x;                 // key tile
-    const int zkv = blockIdx.y;                // b * H_kv + kv head
+    // causal: key tile jt has the query tiles from jt on, so the grid runs the key tiles in the slow
+    // dimension and the costliest (first) key tiles of every head start first
+    const int jt = p.causal ? blockIdx.y : blockIdx.x;   // key tile
+    const int zkv = p.causal ? blockIdx.x : blockIdx.y;  // b * H_kv + kv head
     const int b = zkv / p.H_kv, hk = zkv - b * p.H_kv;
     const int N = p.N;
     int kv_valid = N;
@@ -381,10 +383,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 // its S^T, dP^T products overlap the current tile's P/dS work and dV, dK, dQ products. Per step s
 // (query tile i of one head of the group) the MMA warp issues S^T(s), dP^T(s) (M = 128 keys, N = 64
 // queries), then the second-phase products of step s - 1: dV += P^T dO, dK += dS^T Q (which release
-// the ring stage), dQ^T = K^T dS^T (M = d, N = 64 queries) into one of two TMEM buffers. Warps 0-7
-// compute P^T, dS^T (one key row per thread, 32 queries each), then read dQ^T of the previous step
-// for the same 32 queries (one dimension per thread), stage it as two [16 queries][32 dims] boxes
-// and reduce them into dQ.
+// the ring stage), dQ^T = K^T dS^T (M = d, N = 64 queries) into one of two TMEM buffers. 512 threads:
+// warps 0-7 compute P^T, dS^T (one key row per thread, 32 queries each); warps 8-11 (a warpgroup of
+// their own, one TMEM lane quarter = 32 dimensions each) read dQ^T of each step, stage it as four
+// [16 queries][32 dims] boxes through two buffers and reduce them into dQ, while warps 0-7 already
+// work on the next step; warp 12 issues the MMAs, warp 13 loads.
 // ---------------------------------------------------------------------------------------------
 struct Bw2Cfg {
     static constexpr int D = 128;
@@ -396,7 +399,7 @@ struct Bw2Cfg {
     static constexpr int STAGE = 2 * QD + 1024;          // Q, dO, then lse2[64], dvec[64]
     static constexpr int OFF_PT = OFF_RING + STAGES * STAGE;  // P^T [128 keys][64 queries] bf16 (128 B rows)
     static constexpr int OFF_DST = OFF_PT + 16384;       // dS^T, same layout
-    static constexpr int OFF_DQS = OFF_DST + 16384;      // 8 warps x [16 queries][32 dims] fp32, swizzled
+    static constexpr int OFF_DQS = OFF_DST + 16384;      // 4 warps x 2 buffers x [16 queries][32 dims] fp32, swizzled
     static constexpr int SMEM = 1024 + OFF_DQS + 8 * 2048;
     static constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 256, T_DK = 384;  // dQ^T: 2 x 64 columns
     static constexpr uint32_t IDESC_SD = idesc_f16(128, 64, 1, 1, 0, 0);   // S^T, dP^T: K-major A and B
@@ -404,9 +407,13 @@ struct Bw2Cfg {
     static constexpr uint32_t IDESC_Q = idesc_f16(128, 64, 1, 1, 1, 1);    // dQ^T: A (K^T), B (dS^T) MN-major
 };
 static_assert(Bw2Cfg::SMEM <= 232448, "shared memory");
+constexpr int Q64_THREADS = 512;
+constexpr int Q64_DQ_WARP0 = 8;   // warps 8-11: dQ read-out
+constexpr int Q64_MMA_WARP = 12;
+constexpr int Q64_TMA_WARP = 13;
 static_assert(Bw2Cfg::OFF_PT % 1024 == 0 && Bw2Cfg::OFF_DQS % 1024 == 0 && Bw2Cfg::STAGE % 1024 == 0, "align");
 
-__global__ void __launch_bounds__(BW_THREADS, 1)
+__global__ void __launch_bounds__(Q64_THREADS, 1)
     attn_bwd_q64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                         const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdParams p) {
@@ -420,8 +427,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int jt = blockIdx.x;                 // key tile (128 keys)
-    const int zkv = blockIdx.y;                // b * H_kv + kv head
+    const int jt = p.causal ? blockIdx.y : blockIdx.x;   // key tile (128 keys); causal: costliest first
+    const int zkv = p.causal ? blockIdx.x : blockIdx.y;  // b * H_kv + kv head
     const int b = zkv / p.H_kv, hk = zkv - b * p.H_kv;
     const int N = p.N;
     int kv_valid = N;
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const int n_steps = n_i * p.group;
     const uint64_t limit_ns = p.wait_limit_ns;
 
-    if (warp == BW_MMA_WARP) {
+    if (warp == Q64_MMA_WARP) {
         tmem_alloc(&tmem_base_sh, 512);
         tmem_relinquish();
     }
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_dq_full[i], 1);
-            mbar_init(&bar_dq_free[i], 256);
+            mbar_init(&bar_dq_free[i], 128);
         }
         mbar_init(&bar_s_full, 1);
         mbar_init(&bar_sdp_free, 256);
@@ -469,7 +476,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     // step s uses ring stage s % 3 for the (s / 3)-th time: that use's barrier phase parity is (s / 3) & 1
     auto stage_ptr = [&](int s) { return smem + C::OFF_RING + (s % C::STAGES) * C::STAGE; };
 
-    if (warp == BW_TMA_WARP) {
+    if (warp == Q64_TMA_WARP) {
         // ================================ TMA producer (one lane) ================================
         if (elect_one() && n_steps > 0) {
             mbar_arrive_expect_tx(&bar_kv, 2 * 32768);
@@ -504,7 +511,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == BW_MMA_WARP) {
+    } else if (warp == Q64_MMA_WARP) {
         // ======================================= MMA issuer =======================================
         auto wait_all = [&](uint64_t* bar, uint32_t parity, uint32_t bit) {
             const bool got = mbar_wait(bar, parity, limit_ns, &abort_flag);
@@ -575,6 +582,50 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         volatile int never = 0;
         const bool drained = mbar_wait(&bar_done, 0, limit_ns, &never);
         if (!__all_sync(0xffffffffu, drained) && lane == 0) bw_fail(&abort_flag, ERRBIT_WAIT_DRAIN);
+    } else if (warp >= Q64_DQ_WARP0 && warp < Q64_DQ_WARP0 + 4) {
+        // ===== warps 8-11: dQ of every step. This warp's TMEM lanes are dimensions 32 wq .. 32 wq + 31
+        // (one per thread) of dQ^T; its 64 query columns leave as four [16 queries][32 dims] boxes,
+        // staged 128-byte swizzled through two 2 KB buffers and added into the fp32 dQ by bulk tensor
+        // reductions (rows past N are not written) =====
+        const int wq = warp & 3;
+        const uint32_t lane_off = tmem_lane_base(warp);
+        const uint32_t stage = smem_u32(smem + C::OFF_DQS + (warp - Q64_DQ_WARP0) * 4096);
+        const uint32_t colb = (lane & 3) * 4;
+        for (int t = 0; t < n_steps; ++t) {
+            const bool got = mbar_wait(&bar_dq_full[t & 1], (t >> 1) & 1, limit_ns, &abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_O);
+                break;
+            }
+            tc_fence_after();
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tmem + lane_off + C::T_DQ + 64 * (t & 1), v0);
+            tmem_ld32(tmem + lane_off + C::T_DQ + 64 * (t & 1) + 32, v1);
+            tmem_wait_ld(v0);
+            tmem_wait_ld(v1);
+            tc_fence_before();
+            mbar_arrive(&bar_dq_free[t & 1]);  // the MMA warp may write this buffer's next dQ^T
+            const int bh = b * p.H + step_head(t), it = step_tile(t);
+#pragma unroll
+            for (int hq = 0; hq < 4; ++hq) {  // queries 16 hq .. 16 hq + 15
+                const uint32_t buf = stage + (hq & 1) * 2048;
+                if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous box was read
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    st_shared_f32(buf + q * 128 + ((((lane >> 2) ^ (q & 7))) << 4) + colb,
+                                  __uint_as_float(hq < 2 ? v0[16 * hq + q] : v1[16 * (hq - 2) + q]) * p.scale);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_3d(&tmDQ, smem + (buf - smem_u32(smem)), wq * 32, it * C::QT + 16 * hq, bh);
+                    bulk_commit_group();
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0) bulk_wait_group_all();  // every reduction of this warp performed
+        __syncwarp();
     } else if (warp < 8) {
         // ===== warps 0-7: one key row each, 32 queries (warps 0-3: queries 0-31, warps 4-7: 32-63) =====
         const int qh = warp >> 2;
@@ -585,43 +636,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const float sl = p.scale_log2;
         const uint32_t pt_row = smem_u32(smem + C::OFF_PT) + r * 128;
         const uint32_t dst_row = smem_u32(smem + C::OFF_DST) + r * 128;
-        const uint32_t stage = smem_u32(smem + C::OFF_DQS + warp * 2048);
         bool ok = true;
-        // dQ of step t for this warp's 32 queries: dQ^T from tensor memory (this thread: dimension
-        // 32 wq + lane), staged as two [16 queries][32 dims] boxes (128-byte swizzled), reduced into dQ
-        auto dq_out = [&](int t) -> bool {
-            const bool got = mbar_wait(&bar_dq_full[t & 1], (t >> 1) & 1, limit_ns, &abort_flag);
-            if (!__all_sync(0xffffffffu, got)) {
-                if (!got) bw_fail(&abort_flag, ERRBIT_WAIT_O);
-                return false;
-            }
-            tc_fence_after();
-            uint32_t v0[32];
-            tmem_ld32(tmem + lane_off + C::T_DQ + 64 * (t & 1) + 32 * qh, v0);
-            tmem_wait_ld(v0);
-            tc_fence_before();
-            mbar_arrive(&bar_dq_free[t & 1]);
-            const uint32_t colb = (lane & 3) * 4;
-            const int bh = b * p.H + step_head(t), it = step_tile(t);
-#pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {  // queries 32 qh + 16 hq .. + 15: one 32 x 16 box each
-                if (lane == 0) bulk_wait_group_read<0>();  // the staging buffer's previous box was read
-                __syncwarp();
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    st_shared_f32(stage + q * 128 + ((((lane >> 2) ^ (q & 7))) << 4) + colb,
-                                  __uint_as_float(v0[16 * hq + q]) * p.scale);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {  // rows past N are not written by the reduction
-                    tma_reduce_add_3d(&tmDQ, smem + C::OFF_DQS + warp * 2048, wq * 32,
-                                      it * C::QT + 32 * qh + 16 * hq, bh);
-                    bulk_commit_group();
-                }
-                __syncwarp();
-            }
-            return true;
-        };
         for (int s = 0; s < n_steps && ok; ++s) {
             const int it = step_tile(s);
             const int q0 = it * C::QT + 32 * qh;
@@ -678,14 +693,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             fence_proxy_async_smem();  // the MMAs read P^T and dS^T through the async proxy
             tc_fence_before();
             mbar_arrive(&bar_ps_full);
-            if (s > 0 && !dq_out(s - 1)) {
-                ok = false;
-                break;
-            }
         }
-        if (ok && n_steps > 0 && !dq_out(n_steps - 1)) ok = false;
-        if (lane == 0) bulk_wait_group_all();  // every reduction of this warp performed
-        __syncwarp();
         // ---- dK, dV of this key tile (warps 0-3): fp32 rows straight to device memory ----
         if (qh == 0 && ok && n_steps > 0) {
             const bool got = mbar_wait(&bar_done, 0, limit_ns, &abort_flag);
@@ -728,7 +736,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == BW_MMA_WARP) {
+    if (warp == Q64_MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -774,7 +782,8 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tmQ, const CUtensorMap& tmK, 
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
     }
-    const dim3 grid(static_cast<unsigned>(p.n_qt), static_cast<unsigned>(p.B * p.H_kv));
+    const dim3 grid = p.causal ? dim3(static_cast<unsigned>(p.B * p.H_kv), static_cast<unsigned>(p.n_qt))
+                               : dim3(static_cast<unsigned>(p.n_qt), static_cast<unsigned>(p.B * p.H_kv));
     attn_bwd_tc_kernel<D><<<grid, BW_THREADS, BwCfg<D>::SMEM, stream>>>(tmQ, tmK, tmV, tmDO, tmDQ, p);
     return cudaGetLastError();
 }
@@ -784,7 +793,7 @@ cudaError_t launch_attn_bwd(int d, const BwdPrepParams& prep, const CUtensorMap&
                             const BwdParams& p, cudaStream_t stream) {
     const long long rows = static_cast<long long>(prep.rows) * prep.NQP;
     const long long blocks = (rows + 7) / 8;
-    if (blocks > 0x7fffffffLL || p.B * p.H_kv > 65535) return cudaErrorInvalidConfiguration;
+    if (blocks > 0x7fffffffLL || p.B * p.H_kv > 65535 || p.n_qt > 65535) return cudaErrorInvalidConfiguration;
     attn_bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(prep);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -798,8 +807,9 @@ cudaError_t launch_attn_bwd(int d, const BwdPrepParams& prep, const CUtensorMap&
             if (e != cudaSuccess) return e;
             if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
         }
-        const dim3 grid(static_cast<unsigned>(p.n_qt), static_cast<unsigned>(p.B * p.H_kv));
-        attn_bwd_q64_kernel<<<grid, BW_THREADS, Bw2Cfg::SMEM, stream>>>(tmQ, tmK, tmV, tmDO, tmDQ, p);
+        const dim3 grid = p.causal ? dim3(static_cast<unsigned>(p.B * p.H_kv), static_cast<unsigned>(p.n_qt))
+                                   : dim3(static_cast<unsigned>(p.n_qt), static_cast<unsigned>(p.B * p.H_kv));
+        attn_bwd_q64_kernel<<<grid, Q64_THREADS, Bw2Cfg::SMEM, stream>>>(tmQ, tmK, tmV, tmDO, tmDQ, p);
         return cudaGetLastError();
     }
     if (d == 64) return launch_bwd_t<64>(tmQ, tmK, tmV, tmDO, tmDQ, p, stream);
