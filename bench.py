@@ -553,6 +553,28 @@ def run_ours(args, w):
     return 0
 
 
+def run_launch_list(args):
+    """Three plain attn_fwd calls per workload, every workload in turn (inputs drawn on the device),
+    for a profiler's launch list: the kernels appear in workload order, two launches per bf16 call
+    (the V pre-pass, then the attention kernel) and one per fp32 call."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from exact_tiled_attention_50_b300 import attn
+    for name, w in inputs.WORKLOADS.items():
+        x = inputs.make_inputs_device(w, dev)
+        prob = Problem(attn, w, x, dev)
+        step = prob.step_fn("bf16")
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        rc = attn.check()
+        print(json.dumps({"workload": name, "calls": 3, "launches_per_call": attn.launches_per_call(x.q.dtype),
+                          "status": attn.status_string(rc)}), flush=True)
+        del prob, x
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -568,11 +590,15 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other paths, the per-workload device times and the one-core oracle timings")
     ap.add_argument("--extra-steps", type=int, default=20, help="timed steps of each other path in the extras")
+    ap.add_argument("--launch-list", action="store_true",
+                    help="no timing: three calls of every workload in turn, for a profiler's launch list")
     ap.add_argument("--path", choices=["bf16", "fp8", "bias_dropout", "dropout", "bwd"], default="bf16",
                     help="bf16 tensor-core path (the headline) or the fp8 path with incoherent processing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.launch_list:
+        return run_launch_list(args)
     w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -21,7 +21,7 @@ EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_workspace_byte
             "attn_debug_set_wait_limit_ns", "attn_debug_set_skip_kv_load", "attn_set_kernel_events",
             "attn_event_elapsed_ms", "attn_fwd_noalloc", "attn_debug_schedule",
             "attn_debug_last_error_bits", "attn_merge", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_fp8",
-            "attn_fwd_fp8_workspace_bytes", "attn_fwd_ex")
+            "attn_fwd_fp8_workspace_bytes", "attn_fwd_ex", "attn_debug_set_plan_mode")
 
 
 class AttnError(RuntimeError):
@@ -66,6 +66,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_debug_set_wait_limit_ns.restype = None
     lib.attn_debug_set_skip_kv_load.argtypes = [ci]
     lib.attn_debug_set_skip_kv_load.restype = None
+    lib.attn_debug_set_plan_mode.argtypes = [ci]
+    lib.attn_debug_set_plan_mode.restype = None
     lib.attn_set_kernel_events.argtypes = [vp, vp]
     lib.attn_set_kernel_events.restype = None
     lib.attn_debug_last_error_bits.argtypes = []

@@ -19,6 +19,7 @@ namespace {
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;  // 1 s
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int> g_skip_kv_load{0};
+std::atomic<int> g_plan_mode{0};
 std::atomic<uint32_t> g_last_error_bits{0};
 std::atomic<cudaEvent_t> g_ev_start{nullptr};
 std::atomic<cudaEvent_t> g_ev_stop{nullptr};
@@ -246,7 +247,7 @@ attn_status run_bf16_path(const void* Q, const void* K, const void* V, void* O, 
     p.boff = reinterpret_cast<const long long*>(ws + w.boff);
     p.part = reinterpret_cast<float*>(ws + w.part);
     p.flags = reinterpret_cast<unsigned int*>(ws + w.flags);
-    p.plan = attn_impl::make_plan(B, H, N, causal, kv_len != nullptr, sms);
+    p.plan = attn_impl::make_plan(B, H, N, causal, kv_len != nullptr, sms, g_plan_mode.load());
     p.H_kv = H_kv;
     p.group = H / H_kv;
     p.scale_log2 = scale * 1.4426950408889634f;
@@ -425,7 +426,7 @@ attn_status attn_fwd_fp8(const void* Q, const void* K, const void* V, float* O, 
     p.boff = reinterpret_cast<const long long*>(ws + w.boff);
     p.part = reinterpret_cast<float*>(ws + w.part);
     p.flags = reinterpret_cast<unsigned int*>(ws + w.flags);
-    p.plan = attn_impl::make_plan(B, H, N, causal, kv_len != nullptr, sms);
+    p.plan = attn_impl::make_plan(B, H, N, causal, kv_len != nullptr, sms, g_plan_mode.load());
     p.H_kv = H_kv;
     p.group = H / H_kv;
     // the two unnormalised rotations multiply every score by d (a power of two here)
@@ -540,11 +541,14 @@ void attn_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns :
 
 void attn_debug_set_skip_kv_load(int on) { g_skip_kv_load.store(on ? 1 : 0); }
 
+void attn_debug_set_plan_mode(int mode) { g_plan_mode.store(mode == 1 || mode == 2 ? mode : 0); }
+
 int attn_debug_schedule(int B, int H, int N, int causal, const int32_t* kv_len_host, int sms, int32_t* out,
                         int max_segments) {
     if (B <= 0 || H <= 0 || N <= 0 || sms <= 0 || max_segments < 0 || (!out && max_segments > 0)) return -1;
     if (attn_impl::plan_max_steps(B, H, N, causal ? 1 : 0) >= 0x7fffffffLL) return -1;
-    const attn_impl::SchedPlan plan = attn_impl::make_plan(B, H, N, causal ? 1 : 0, kv_len_host != nullptr, sms);
+    const attn_impl::SchedPlan plan =
+        attn_impl::make_plan(B, H, N, causal ? 1 : 0, kv_len_host != nullptr, sms, g_plan_mode.load());
     std::vector<int> nb(B);
     std::vector<long long> boff(B + 1, 0);
     for (int b = 0; b < B; ++b) {

@@ -38,9 +38,12 @@ enum : uint32_t {
 // ---------------------------------------------------------------------------------------------
 constexpr int SCHED_MAX_CTAS = 160;  // partial-result slots reserved in the workspace
 constexpr int SCHED_MIN_STEPS = 2;   // the CTA count is capped so that chunks hold at least this many steps
-// Extra time of a split unit, in key steps: the owner waits for the later pieces' partial results and
-// reads them back before its epilogue. The plan splits units only when that saves more than this.
-constexpr int SCHED_SPLIT_PENALTY = 4;
+// Extra time of a stream-K plan, in key steps: its CTAs run more segments (each with a Q load and an
+// epilogue) and the owners of split units wait for and merge the other pieces' partial results.
+// Measured on B300 against whole-unit plans (B1 H16 d128, N = 512 ... 16384, causal and not): splitting
+// lost by 6-10 steps' worth on small problems and won by about 30 steps at N = 8192; the plan splits
+// units only when that saves more than this.
+constexpr int SCHED_SPLIT_PENALTY = 10;
 
 enum : int { SEG_COMPLETE = 0, SEG_OWNER = 1, SEG_WRITER = 2 };
 
@@ -279,7 +282,8 @@ cudaError_t launch_attn_tc(int d, bool out_bf16, const CUtensorMap& tmQ, const C
                            const CUtensorMap& tmV16, const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream);
 
 // Persistent-CTA plan for these sizes on a device with `sms` SMs (kv_len given or not).
-SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms);
+// mode: 0 = the cheaper plan by the cost model, 1 = whole units in rounds, 2 = stream-K (test hook)
+SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms, int mode = 0);
 long long plan_max_steps(int B, int H, int N, int causal);
 cudaError_t launch_attn_f32(int d, const F32Params& p, cudaStream_t stream);
 

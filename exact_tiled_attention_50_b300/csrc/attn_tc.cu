@@ -1478,7 +1478,7 @@ long long plan_max_steps(int B, int H, int N, int causal) {
     return static_cast<long long>(B) * H * pair_prefix(n_pairs, key_tiles(N), N, causal);
 }
 
-SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms) {
+SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms, int mode) {
     SchedPlan p{};
     p.B = B;
     p.H = H;
@@ -1508,7 +1508,7 @@ SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms) {
     }
     const long long rounds = (units + g_cap - 1) / g_cap;
     const long long t_whole = uniform ? rounds * nb : (rounds == 1 ? max_cost : -1);
-    if (t_whole >= 0 && t_whole <= t_stream) {
+    if (mode == 1 || (mode == 0 && t_whole >= 0 && t_whole < t_stream)) {
         p.R_dp = static_cast<int>(rounds);
         p.G = static_cast<int>((units + rounds - 1) / rounds);  // the fewest CTAs for that many rounds
         p.sk = 0;

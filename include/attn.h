@@ -219,6 +219,14 @@ void attn_debug_set_wait_limit_ns(uint64_t ns);
 void attn_debug_set_skip_kv_load(int on);
 
 /*
+ * Test hook: the work plan of the following calls' persistent kernel (and of attn_debug_schedule).
+ * 0 (default) = the cheaper of the two plans by the library's cost model; 1 = whole work units in
+ * rounds (no unit split between CTAs); 2 = stream-K (the key range shared evenly, split units merged).
+ * Results are the same under every plan; only the time differs. Other values mean 0.
+ */
+void attn_debug_set_plan_mode(int mode);
+
+/*
  * Test hook (host only, no GPU needed): the work schedule the tensor-core kernel would follow for
  * these sizes on a device with `sms` SMs, with kv_len given as a HOST int32 array [B] (or NULL).
  * Writes up to max_segments records (out may be NULL when max_segments is 0) of 8 int32 (cta, b, h, pair, k0, k1, cost, kind; kind 0 = the

@@ -228,3 +228,18 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
         attn.lib.attn_debug_set_wait_limit_ns(0)
     assert attn.check() == attn.ATTN_OK  # the error word was cleared
     parity.check_full(x, "bf16", what="after timeout")
+
+
+# ---------------------------------------------------------------- both work plans
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("causal", [False, True])
+def test_both_work_plans_match_the_oracle(mode, causal):
+    """Whole units in rounds (mode 1) and stream-K with split units merged (mode 2) give the same
+    attention, whichever the cost model would pick for the shape."""
+    from exact_tiled_attention_50_b300 import attn
+    x = inputs.custom(2, 8, 2, 1000, 128, causal=causal, padded=True, peaky=True, seed=300 + mode)
+    attn.lib.attn_debug_set_plan_mode(mode)
+    try:
+        parity.check_full(x, "bf16", what=f"plan mode {mode} causal={causal}")
+    finally:
+        attn.lib.attn_debug_set_plan_mode(0)

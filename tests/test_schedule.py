@@ -82,7 +82,7 @@ def test_schedule_covers_every_key_step_once(attn, B, H, N, causal, kv_len, sms)
             assert all(p[3] == WRITER for p in pieces[1:])
 
 
-SPLIT_PENALTY = 4  # key steps a split unit costs its owner (the plan's cost model)
+SPLIT_PENALTY = 10  # key steps a stream-K plan costs beyond its even share (the plan's cost model)
 
 
 def plan_kind(segs):
@@ -139,7 +139,7 @@ def model_makespans(B, H, N, causal, padded, sms):
 def test_schedule_takes_the_cheaper_plan(attn, B, H, N, causal, kv_len, sms):
     segs = attn.schedule(B, H, N, causal, kv_len, sms)
     t_whole, t_stream = model_makespans(B, H, N, causal, kv_len is not None, sms)
-    want = "whole" if t_whole is not None and t_whole <= t_stream else "stream"
+    want = "whole" if t_whole is not None and t_whole < t_stream else "stream"
     got = plan_kind(segs)
     # a stream-K plan whose chunk boundaries all fall on unit boundaries splits nothing: it looks whole
     assert got == want or (want == "stream" and got == "whole")
@@ -149,6 +149,8 @@ def test_schedule_takes_the_cheaper_plan(attn, B, H, N, causal, kv_len, sms):
     (4, 8, 1024, False, None, 128, "whole"),       # 128 units of 8 steps: one round, no merges
     (1, 16, 512, False, None, 32, "whole"),        # 32 units of 4 steps
     (1, 16, 512, True, None, 32, "whole"),
+    (1, 16, 1024, True, None, 64, "whole"),        # causal: the costliest unit (8 steps) beats 3 + merges
+    (1, 16, 2048, False, None, 128, "whole"),
     (1, 16, 8192, False, None, 148, "stream"),     # 512 units of 64 steps: 3.46 rounds -> stream-K
     (1, 16, 16384, False, None, 148, "stream"),
     (2, 32, 8192, True, None, 148, "stream"),
