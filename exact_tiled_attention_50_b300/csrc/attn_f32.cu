@@ -7,10 +7,10 @@
 // log-sum-exp (safe_softmax_block listing of "AI训练的最大障碍不是算力,而是'内存墙'", zsdodo.com;
 // section 4.1.3 of "第四章 注意力机制实战案例", aiknowledge.cn).
 //
-// Mapping: a CTA of 256 threads (8 warps) owns 8 query rows of one (b, h) and splits the key range
-// into 8 slices, one per warp, so that short sequences still spread over many warps: in a warp, four
+// Mapping: a CTA of 16 warps (d = 64) or 8 (d = 128) owns 8 query rows of one (b, h) and splits the
+// key range into one slice per warp, so that short sequences still spread over many warps: in a warp, four
 // consecutive lanes share a row and each holds a quarter of its query and output columns. Every warp
-// runs the online softmax over its slice (key rows read straight from L2, 8 or 4 at a time); the 8 partial
+// runs the online softmax over its slice (key rows read straight from L2, 4 at a time); the partial
 // results of a row are then combined in shared memory with the softmax merge rule (formula 2 of
 // "闪电注意力的数学原理" on the unite.ai page: m = max m_w, l = sum l_w e^(m_w - m), O = sum O_w
 // e^(m_w - m) / l).
@@ -24,14 +24,21 @@ namespace attn_impl {
 
 namespace {
 constexpr int F32_ROWS = 8;      // query rows per CTA
-constexpr int F32_WARPS = 8;     // key slices per CTA
-constexpr int F32_THREADS = 32 * F32_WARPS;
+// key slices (warps) per CTA: 16 at d = 64, 8 at d = 128 (the merge buffer, 16 or 8 x 8 rows x d fp32,
+// stays at 32 KB)
+template <int D>
+struct F32Cfg {
+    static constexpr int WARPS = D == 64 ? 16 : 8;
+    static constexpr int THREADS = 32 * WARPS;
+};
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(F32_THREADS) attn_fwd_f32_kernel(const F32Params p) {
+__global__ void __launch_bounds__(F32Cfg<D>::THREADS, 1) attn_fwd_f32_kernel(const F32Params p) {
+    constexpr int F32_WARPS = F32Cfg<D>::WARPS;
+    constexpr int F32_THREADS = F32Cfg<D>::THREADS;
     constexpr int CPL = D / 4;            // columns per lane
-    constexpr int CH = D == 64 ? 8 : 4;   // keys per online-softmax update (their rows held in registers)
+    constexpr int CH = 4;                 // keys per online-softmax update (their rows held in registers)
     __shared__ __align__(16) float sm_o[F32_WARPS][F32_ROWS][D];
     __shared__ float sm_m[F32_WARPS][F32_ROWS], sm_l[F32_WARPS][F32_ROWS];
     __shared__ float sm_w[F32_WARPS][F32_ROWS], sm_inv[F32_ROWS], sm_lse[F32_ROWS];
@@ -174,9 +181,9 @@ cudaError_t launch_attn_f32(int d, const F32Params& p, cudaStream_t stream) {
     dim3 grid((p.N + F32_ROWS - 1) / F32_ROWS, p.B * p.H);
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
     if (d == 64)
-        attn_fwd_f32_kernel<64><<<grid, F32_THREADS, 0, stream>>>(p);
+        attn_fwd_f32_kernel<64><<<grid, F32Cfg<64>::THREADS, 0, stream>>>(p);
     else if (d == 128)
-        attn_fwd_f32_kernel<128><<<grid, F32_THREADS, 0, stream>>>(p);
+        attn_fwd_f32_kernel<128><<<grid, F32Cfg<128>::THREADS, 0, stream>>>(p);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();
