@@ -21,7 +21,8 @@ EXPORTED = ("attn_fwd", "attn_check", "attn_status_string", "attn_workspace_byte
             "attn_debug_set_wait_limit_ns", "attn_debug_set_skip_kv_load", "attn_set_kernel_events",
             "attn_event_elapsed_ms", "attn_fwd_noalloc", "attn_debug_schedule",
             "attn_debug_last_error_bits", "attn_merge", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_fp8",
-            "attn_fwd_fp8_workspace_bytes", "attn_fwd_ex", "attn_debug_set_plan_mode")
+            "attn_fwd_fp8_workspace_bytes", "attn_fwd_ex", "attn_debug_set_plan_mode", "attn_fwd_host",
+            "attn_fwd_host_groups")
 
 
 class AttnError(RuntimeError):
@@ -40,6 +41,11 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd.restype = ci
     lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci, ci, vp]
     lib.attn_fwd_noalloc.restype = ci
+    lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, ci, ci,
+                                  vp, vp, vp, vp, vp, vp, vp, sz, ci, vp]
+    lib.attn_fwd_host.restype = ci
+    lib.attn_fwd_host_groups.argtypes = [ci, ci, ci]
+    lib.attn_fwd_host_groups.restype = ci
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, vp, sz, vp]
     lib.attn_bwd.restype = ci
     ll = ctypes.c_longlong
@@ -270,6 +276,47 @@ def attn_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: tor
                               _dtype_code(q.dtype), _dtype_code(out.dtype), stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_noalloc")
+
+
+def attn_fwd_host(q_h: torch.Tensor, k_h: torch.Tensor, v_h: torch.Tensor, o_h: torch.Tensor,
+                  lse_h: Optional[torch.Tensor], q_d: torch.Tensor, k_d: torch.Tensor, v_d: torch.Tensor,
+                  o_d: torch.Tensor, lse_d: Optional[torch.Tensor], *, scale: Optional[float] = None,
+                  causal: bool = False, kv_len_h: Optional[torch.Tensor] = None,
+                  kv_len_d: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  n_groups: int = 0) -> None:
+    """attn_fwd with host inputs and outputs, copies and compute pipelined over groups of heads.
+
+    q_h, k_h, v_h, o_h, lse_h (and kv_len_h): contiguous CPU tensors (pinned for overlap) of the shapes
+    and dtypes attn_fwd takes and returns; q_d .. lse_d (and kv_len_d): contiguous CUDA tensors of the
+    same shapes. On return the work is enqueued on the current stream; o_h and lse_h hold the result
+    once that stream reaches this point."""
+    for name, t in (("q_h", q_h), ("k_h", k_h), ("v_h", v_h), ("o_h", o_h)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    for name, t in (("q_d", q_d), ("k_d", k_d), ("v_d", v_d), ("o_d", o_d)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    B, H, N, d = q_h.shape
+    H_kv = k_h.shape[1]
+    if q_d.shape != q_h.shape or k_d.shape != k_h.shape or v_d.shape != v_h.shape or o_d.shape != o_h.shape:
+        raise ValueError("host and device tensors differ in shape")
+    if (lse_h is None) != (lse_d is None) or (kv_len_h is None) != (kv_len_d is None):
+        raise ValueError("give lse (and kv_len) on both sides or on neither")
+    if scale is None:
+        scale = d ** -0.5
+    ws_bytes = workspace_bytes(B, H, H_kv, N, d, q_h.dtype)
+    if workspace is None and ws_bytes > 0:
+        workspace = _workspace(ws_bytes, q_d.device)
+    stream = torch.cuda.current_stream(q_d.device).cuda_stream
+    ptr = (lambda t: t.data_ptr() if t is not None else None)
+    rc = lib.attn_fwd_host(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), ptr(lse_h), B, H, H_kv, N,
+                           d, float(scale), int(bool(causal)), ptr(kv_len_h), _dtype_code(q_h.dtype),
+                           _dtype_code(o_h.dtype), q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(), o_d.data_ptr(),
+                           ptr(lse_d), ptr(kv_len_d), ptr(workspace),
+                           workspace.numel() * workspace.element_size() if workspace is not None else 0,
+                           int(n_groups), stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host")
 
 
 def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, do: torch.Tensor,

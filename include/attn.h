@@ -169,6 +169,37 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const float* O
                      const int32_t* kv_len, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * attn_fwd for inputs and outputs in host memory: the copies to the device, the attention and the
+ * copies back are pipelined over groups of heads (heads are independent, so a group of key/value
+ * heads with their query heads is copied in, computed and copied back on its own), and group k's
+ * inputs cross PCIe while group k - 1 is computed and group k - 2's outputs cross back. Each group's
+ * attention is an attn_fwd call on slices of the device buffers, so the results are attn_fwd's.
+ *   Q_h, K_h, V_h, O_h, LSE_h, kv_len_h   host pointers, layouts and types as attn_fwd (LSE_h and
+ *                kv_len_h may be NULL, then LSE_d / kv_len_d must be NULL too). Page-locked host
+ *                memory lets the copies run asynchronously and overlap; pageable memory still works.
+ *   Q_d, K_d, V_d, O_d, LSE_d, kv_len_d   device buffers of the same sizes, owned by the caller; they
+ *                hold the inputs and outputs afterwards
+ *   workspace    device, at least attn_workspace_bytes() of one group (the whole problem's size is
+ *                always enough), 256-byte aligned, as for attn_fwd
+ *   n_groups     head groups to aim for (0: 8); never more than 64, and a group never spans two
+ *                batches: attn_fwd_host_groups() gives the number the call will use
+ *   stream       the call's stream: the inputs are read after the work already on it, the kernels run
+ *                on it, and it reaches the end of the call once every output is back in host memory
+ *                (the copies run on two streams the library creates per device on first use and keeps)
+ * Errors as attn_fwd (checked before anything is enqueued where possible); ATTN_ERR_CUDA if a copy or
+ * stream operation fails. Two calls on different streams share the copy streams and run one after
+ * the other; calls that share device buffers or a workspace must not overlap.
+ */
+attn_status attn_fwd_host(const void* Q_h, const void* K_h, const void* V_h, void* O_h, float* LSE_h, int B, int H,
+                          int H_kv, int N, int d, float scale, int causal, const int32_t* kv_len_h, attn_dtype in_dtype,
+                          attn_dtype out_dtype, void* Q_d, void* K_d, void* V_d, void* O_d, float* LSE_d,
+                          int32_t* kv_len_d, void* workspace, size_t workspace_bytes, int n_groups,
+                          cudaStream_t stream);
+
+/* Number of head groups attn_fwd_host uses for these sizes and n_groups (-1 on invalid sizes). */
+int attn_fwd_host_groups(int B, int H_kv, int n_groups);
+
+/*
  * Merge of attention results over disjoint key sets (split-KV or sequence-parallel attention: each
  * part attends the same queries to its own keys). For every row,
  *     LSE = log(sum_i exp(LSE_i)),   O = sum_i exp(LSE_i - LSE) O_i
