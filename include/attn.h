@@ -169,7 +169,9 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const float* O
                      const int32_t* kv_len, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * attn_fwd for inputs and outputs in host memory: the copies to the device, the attention and the
+ * attn_fwd for inputs and outputs in host memory (the operation is attn_fwd's; the overlap of
+ * copies and compute is the asynchronous overlap named in section "闪电注意力-3", item 1, of
+ * "闪电注意力：革命性地提高Transformer效率", unite.ai): the copies to the device, the attention and the
  * copies back are pipelined over groups of heads (heads are independent, so a group of key/value
  * heads with their query heads is copied in, computed and copied back on its own), and group k's
  * inputs cross PCIe while group k - 1 is computed and group k - 2's outputs cross back. Each group's
@@ -187,8 +189,9 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const float* O
  *                on it, and it reaches the end of the call once every output is back in host memory
  *                (the copies run on two streams the library creates per device on first use and keeps)
  * Errors as attn_fwd (checked before anything is enqueued where possible); ATTN_ERR_CUDA if a copy or
- * stream operation fails. Two calls on different streams share the copy streams and run one after
- * the other; calls that share device buffers or a workspace must not overlap.
+ * stream operation fails. Calls on different streams (or host threads) share the copy streams, so
+ * their copies queue behind each other; calls that share device buffers or a workspace must not
+ * overlap.
  */
 attn_status attn_fwd_host(const void* Q_h, const void* K_h, const void* V_h, void* O_h, float* LSE_h, int B, int H,
                           int H_kv, int N, int d, float scale, int causal, const int32_t* kv_len_h, attn_dtype in_dtype,
