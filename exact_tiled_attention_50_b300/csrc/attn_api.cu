@@ -404,6 +404,9 @@ attn_status attn_fwd_fp8(const void* Q, const void* K, const void* V, float* O, 
     fp.n_ktiles = w.n_ktiles;
     fp.heads_q = B * H;
     fp.heads_kv = B * H_kv;
+    fp.sms = device_sms();
+    if (fp.sms <= 0) return ATTN_ERR_CUDA;
+    fp.wait_limit_ns = g_wait_limit_ns.load();
 
     const int npad = w.n_ktiles * 128;
     CUtensorMap tmQ, tmK, tmV, tmO;

@@ -240,6 +240,8 @@ struct Fp8PrepParams {
     int32_t* v_exp;           // [B*H_kv][n_ktiles]
     const int8_t* signs;      // d values +-1 (rotation), or nullptr (no rotation)
     int N, d, n_ktiles, heads_q, heads_kv;
+    int sms;                  // SMs of the device (the pre-pass runs two blocks on each)
+    uint64_t wait_limit_ns;   // bound of the waits for its copies
 };
 
 struct PlanParams {

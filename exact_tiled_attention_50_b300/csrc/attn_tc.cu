@@ -45,6 +45,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "attn_internal.h"
@@ -1212,13 +1213,21 @@ cudaError_t launch_vprep(const VPrepParams& p, const PlanParams& plan, cudaStrea
 }
 
 // ---------------------------------------------------------------------------------------------
-// fp8 pre-pass (d = 128): one block of 512 threads per 128-row tile of Q, K or V, plus the plan block.
+// fp8 pre-pass (d = 128): a persistent grid of 512-thread blocks, two per SM, each taking every G-th
+// 128-row tile of the list (Q tiles, then K tiles, then V tiles), plus one block that plans the
+// schedule. A tile (128 rows x 256 bytes, contiguous in BHND) reaches shared memory by one bulk copy
+// into a two-stage ring: the copy of a block's next tile is in flight while it works on the current
+// one, so the copy engines, not registers, hold the bytes in flight that HBM bandwidth needs.
 // Q and K rows are multiplied by the signs and transformed by the unnormalised Walsh-Hadamard
 // butterflies (spans 1, 2, 4, ..., 64 in that order; each output one fp32 addition or subtraction),
 // then every tile is rounded to E4M3 at its own power-of-two scale. Four threads share a row (32
-// elements each), so that a thread needs few registers and many tiles stream through an SM at once.
+// elements each).
 // ---------------------------------------------------------------------------------------------
 constexpr int FP8P_THREADS = 512;
+constexpr int FP8P_BLOCKS_PER_SM = 2;
+constexpr int FP8P_STAGES = 2;
+constexpr int FP8P_TILE_BYTES = 128 * 128 * 2;               // one bf16 tile, 256 bytes per row
+constexpr int FP8P_SMEM = FP8P_STAGES * FP8P_TILE_BYTES;       // dynamic shared memory of the ring
 
 // Tile exponent from the largest |x| as fp32 bits: max |x| < 2^(e8 - 126); e = max(e8 - 134, -100)
 // keeps the tile's values times 2^-e below 256 = 2^8 (E4M3 holds up to 448); a zero tile gets 0.
@@ -1228,11 +1237,13 @@ __device__ __forceinline__ int fp8_tile_exponent(uint32_t max_abs_bits) {
     return max(e8 - 134, -100);
 }
 
-// Block-wide maximum of non-negative fp32 bit patterns (their order is that of the values).
-__device__ __forceinline__ uint32_t fp8_block_max(uint32_t v, uint32_t* red) {
+// Block-wide maximum of non-negative fp32 bit patterns (their order is that of the values). `bad`
+// (this thread's copy wait gave up) is OR-reduced over the block by the same barrier, so that every
+// thread takes the same decision.
+__device__ __forceinline__ uint32_t fp8_block_max(uint32_t v, uint32_t* red, bool& bad) {
     v = __reduce_max_sync(0xffffffffu, v);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
+    bad = __syncthreads_or(bad) != 0;
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < FP8P_THREADS / 32; ++i) m = max(m, red[i]);
@@ -1242,144 +1253,298 @@ __device__ __forceinline__ uint32_t fp8_block_max(uint32_t v, uint32_t* red) {
 // 2^-e as fp32 for e in [-100, 120]
 __device__ __forceinline__ float fp8_pow2_neg(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
 
-// One 128-row tile of Q or K: thread t holds row t / 4, elements 32 (t mod 4) .. +31. Butterflies of
-// spans 1 .. 16 run inside the thread, span 32 pairs lanes 4r + q and 4r + (q ^ 1), span 64 lanes
-// 4r + q and 4r + (q ^ 2); the lower element of a pair keeps x + y, the upper x - y.
-__device__ void fp8_prep_qk_tile(const __nv_bfloat16* src, uint8_t* dst, int32_t* exp_out, const int8_t* signs,
-                                 int N, int tile, uint32_t* red) {
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// One 128-row tile of Q or K, staged row-major in shared memory: thread t holds row t / 4, elements
+// 32 (t mod 4) .. +31 as sixteen fp32 pairs. The signs are XORed into the bf16 words before they are
+// widened (a sign flip is exact). Butterflies of span 1 run on single values, spans 2 .. 16 on pairs
+// (two-wide fp32 adds and x - y = fma(y, -1, x), both single-rounded like the scalar forms), span 32
+// pairs lanes 4r + q and 4r + (q ^ 1), span 64 lanes 4r + q and 4r + (q ^ 2), each as one fma with a
+// factor of +-1; the lower element of a pair keeps x + y, the upper x - y.
+template <class AfterMax>
+__device__ bool fp8_prep_qk_tile(const uint8_t* stage, uint8_t* dst, int32_t* exp_out, const uint32_t* sgn,
+                                 int N, int tile, uint32_t* red, bool bad, AfterMax after_max) {
     const int q4 = threadIdx.x & 3;
-    const int row = tile * 128 + (threadIdx.x >> 2);
-    float a[32];
+    const int r = threadIdx.x >> 2;
+    const int row = tile * 128 + r;
+    uint32_t w[16];  // bf16 pairs: element 2e in the low half of w[e], element 2e + 1 in the high half
     if (row < N) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * 128 + q4 * 32);
+        // The thread's four 16-byte chunks are read in an order rotated by rot = (q4 >> 1) + 2 (r & 1):
+        // rows lie 256 bytes apart, so without it the eight threads of a quarter warp (rows 2p, 2p + 1,
+        // quarters 0-3) would fall on four bank groups; rotated, they cover all eight at every step.
+        const int rot = ((q4 >> 1) + 2 * (r & 1)) & 3;
+        const uint8_t* base = stage + r * 256 + q4 * 64;
+        uint4 u0 = lds128(base + ((0 + rot) & 3) * 16);
+        uint4 u1 = lds128(base + ((1 + rot) & 3) * 16);
+        uint4 u2 = lds128(base + ((2 + rot) & 3) * 16);
+        uint4 u3 = lds128(base + ((3 + rot) & 3) * 16);
+        if (rot & 1) {  // chunk c is in u[(c - rot) & 3]: rotate back by one, then by two
+            const uint4 t = u3;
+            u3 = u2;
+            u2 = u1;
+            u1 = u0;
+            u0 = t;
+        }
+        if (rot & 2) {
+            uint4 t = u0;
+            u0 = u2;
+            u2 = t;
+            t = u1;
+            u1 = u3;
+            u3 = t;
+        }
+        const uint4 uu[4] = {u0, u1, u2, u3};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const uint4 u = __ldg(s4 + k);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                a[8 * k + 2 * e] = __uint_as_float(w[e] << 16);
-                a[8 * k + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-            }
+            w[4 * k] = uu[k].x;
+            w[4 * k + 1] = uu[k].y;
+            w[4 * k + 2] = uu[k].z;
+            w[4 * k + 3] = uu[k].w;
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) a[i] = 0.f;
+        for (int e = 0; e < 16; ++e) w[e] = 0u;
     }
-    if (signs) {
+    f32x2 b[16];
+    if (sgn) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(sgn + q4 * 16);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) a[i] *= static_cast<float>(__ldg(signs + q4 * 32 + i));
+        for (int k = 0; k < 4; ++k) {
+            const uint4 m = s4[k];
+            w[4 * k] ^= m.x;
+            w[4 * k + 1] ^= m.y;
+            w[4 * k + 2] ^= m.z;
+            w[4 * k + 3] ^= m.w;
+        }
 #pragma unroll
-        for (int h = 1; h < 32; h <<= 1) {
+        for (int e = 0; e < 16; ++e) {  // span 1
+            const float x = __uint_as_float(w[e] << 16), y = __uint_as_float(w[e] & 0xffff0000u);
+            b[e] = make_f32x2(x + y, x - y);
+        }
+        const f32x2 neg1 = make_f32x2(-1.f, -1.f);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                if (i & h) continue;
-                const float x = a[i], y = a[i + h];
-                a[i] = x + y;
-                a[i + h] = x - y;
+        for (int hp = 1; hp < 16; hp <<= 1) {  // spans 2, 4, 8, 16: pairs e and e + span/2
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                if (e & hp) continue;
+                const f32x2 x = b[e], y = b[e + hp];
+                b[e] = add_f32x2(x, y);
+                b[e + hp] = fma_f32x2(y, neg1, x);
             }
         }
+        const float s32 = (q4 & 1) ? -1.f : 1.f, s64 = (q4 & 2) ? -1.f : 1.f;
+        const f32x2 m32 = make_f32x2(s32, s32), m64 = make_f32x2(s64, s64);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {  // span 32
-            const float o = __shfl_xor_sync(0xffffffffu, a[i], 1);
-            a[i] = (q4 & 1) ? o - a[i] : a[i] + o;
+        for (int e = 0; e < 16; ++e) {  // span 32: mine * (+-1) + the partner's
+            float x, y;
+            split_f32x2(b[e], x, y);
+            const f32x2 o = make_f32x2(__shfl_xor_sync(0xffffffffu, x, 1), __shfl_xor_sync(0xffffffffu, y, 1));
+            b[e] = fma_f32x2(b[e], m32, o);
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {  // span 64
-            const float o = __shfl_xor_sync(0xffffffffu, a[i], 2);
-            a[i] = (q4 & 2) ? o - a[i] : a[i] + o;
+        for (int e = 0; e < 16; ++e) {  // span 64
+            float x, y;
+            split_f32x2(b[e], x, y);
+            const f32x2 o = make_f32x2(__shfl_xor_sync(0xffffffffu, x, 2), __shfl_xor_sync(0xffffffffu, y, 2));
+            b[e] = fma_f32x2(b[e], m64, o);
         }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) b[e] = make_f32x2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
     }
-    uint32_t mbits = 0;
+    float mx = 0.f;  // largest |x| (finite inputs)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) mbits = max(mbits, __float_as_uint(a[i]) & 0x7fffffffu);
-    const int e = fp8_tile_exponent(fp8_block_max(mbits, red));
+    for (int e = 0; e < 16; ++e) {
+        float x, y;
+        split_f32x2(b[e], x, y);
+        mx = max3f(mx, fabsf(x), fabsf(y));
+    }
+    const int e = fp8_tile_exponent(fp8_block_max(__float_as_uint(mx), red, bad));
+    if (bad) return false;  // a copy did not land: nothing is written
+    after_max();            // every thread has read the staged tile
     if (threadIdx.x == 0) *exp_out = e;
     const float sc = fp8_pow2_neg(e);
+    const f32x2 sc2 = make_f32x2(sc, sc);
     if (row < N) {
         uint4* d4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * 128 + q4 * 32);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            uint32_t w[4];
+            uint32_t o[4];
 #pragma unroll
             for (int e4 = 0; e4 < 4; ++e4) {
-                const int i = 16 * k + 4 * e4;
-                w[e4] = pack_e4m3x4(a[i] * sc, a[i + 1] * sc, a[i + 2] * sc, a[i + 3] * sc);
+                float x0, x1, x2, x3;
+                split_f32x2(mul_f32x2(b[8 * k + 2 * e4], sc2), x0, x1);
+                split_f32x2(mul_f32x2(b[8 * k + 2 * e4 + 1], sc2), x2, x3);
+                o[e4] = pack_e4m3x4(x0, x1, x2, x3);
             }
-            d4[k] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[k] = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
+    return true;
 }
 
-// One 128-key tile of V, rounded and written transposed: dst row c (dimension c) holds the tile's
-// 128 keys at columns tile*128 ..; keys past N are zero. The tile passes through shared memory with
-// its columns XOR-swizzled by the key's 32-row group, so that the transposed reads of a warp (8
-// dimensions x 4 key groups) fall in distinct banks.
-__device__ void fp8_prep_v_tile(const __nv_bfloat16* src, uint8_t* dstT, int32_t* exp_out, int N, int n_cols,
-                                int tile, uint32_t* red, uint16_t (*sm)[130]) {
+// One 128-key tile of V, staged row-major in shared memory, rounded and written transposed: dst row
+// c (dimension c) holds the tile's 128 keys at columns tile*128 ..; keys past N are zero. The tile
+// is copied once more, into `sm` (rows of 136 halves, 16-byte aligned) with each 8-column chunk moved
+// by an XOR with the key's 16-row group (chunk ^ ((row >> 4) & 7)). Thread t then reads the pair of
+// dimensions 2 (t >> 3), + 1 over keys 16 (t mod 8) .. + 15 as 32-bit words: the eight key groups of
+// a warp land in eight different bank groups.
+constexpr int FP8P_VT_STRIDE = 136;
+template <class AfterMax>
+__device__ bool fp8_prep_v_tile(const uint8_t* stage, uint8_t* dstT, int32_t* exp_out, int N, int n_cols, int tile,
+                                uint32_t* red, uint16_t (*sm)[FP8P_VT_STRIDE], bool bad, AfterMax after_max) {
     uint32_t mbits = 0;  // largest |V| as bf16 bits
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const int idx = threadIdx.x + k * FP8P_THREADS;  // 16-byte vector of the tile: row idx/16
-        const int row = idx >> 4, c8 = ((idx & 15) * 8) ^ ((row >> 5) << 3);
-        uint4 u = make_uint4(0u, 0u, 0u, 0u);
-        if (tile * 128 + row < N)
-            u = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(tile * 128 + row) * 128) + (idx & 15));
+        const int idx = threadIdx.x + k * FP8P_THREADS;  // 16-byte chunk of the tile: row idx/16
+        const int row = idx >> 4, c8 = ((idx & 15) ^ ((row >> 4) & 7)) * 8;
+        const uint4 u = tile * 128 + row < N ? lds128(stage + idx * 16) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(&sm[row][c8]) = u;
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            sm[row][c8 + 2 * q] = static_cast<uint16_t>(w[q] & 0xffffu);
-            sm[row][c8 + 2 * q + 1] = static_cast<uint16_t>(w[q] >> 16);
-            mbits = max(mbits, max(w[q] & 0x7fffu, (w[q] >> 16) & 0x7fffu));
-        }
+        for (int q = 0; q < 4; ++q) mbits = max(mbits, max(w[q] & 0x7fffu, (w[q] >> 16) & 0x7fffu));
     }
-    const int e = fp8_tile_exponent(fp8_block_max(mbits << 16, red));  // (the reduction synchronises sm)
+    const int e = fp8_tile_exponent(fp8_block_max(mbits << 16, red, bad));  // (its barrier synchronises sm)
+    if (bad) return false;
+    after_max();  // every thread has read the staged tile
     if (threadIdx.x == 0) *exp_out = e;
     const float sc = fp8_pow2_neg(e);
-    const int c = threadIdx.x >> 2, kg = threadIdx.x & 3, k0 = kg * 32;  // dimension c, keys k0 .. k0 + 31
-    const int cs = c ^ (kg << 3);                                          // its swizzled column
-    uint32_t o[8];
+    const f32x2 sc2 = make_f32x2(sc, sc);
+    const int cp = threadIdx.x >> 3, kg = threadIdx.x & 7, k0 = kg * 16;  // dimensions 2cp, 2cp + 1
+    // the word of dimensions 2cp, 2cp + 1 in row k0 + j: chunk cp / 4 moved by kg, word cp mod 4
+    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(&sm[k0][(((cp >> 2) ^ kg) << 3) + 2 * (cp & 3)]);
+    uint32_t lo[4], hi[4];  // E4M3 of dimension 2cp (lo) and 2cp + 1 (hi), four keys per word
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        float f[4];
+    for (int q = 0; q < 4; ++q) {
+        float a[4], b[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) f[u] = __uint_as_float(static_cast<uint32_t>(sm[k0 + 4 * q + u][cs]) << 16) * sc;
-        o[q] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+        for (int u = 0; u < 4; u += 2) {
+            const uint32_t w0 = wrow[(4 * q + u) * (FP8P_VT_STRIDE / 2)];
+            const uint32_t w1 = wrow[(4 * q + u + 1) * (FP8P_VT_STRIDE / 2)];
+            split_f32x2(mul_f32x2(make_f32x2(__uint_as_float(w0 << 16), __uint_as_float(w1 << 16)), sc2), a[u],
+                        a[u + 1]);
+            split_f32x2(mul_f32x2(make_f32x2(__uint_as_float(w0 & 0xffff0000u), __uint_as_float(w1 & 0xffff0000u)),
+                                  sc2),
+                        b[u], b[u + 1]);
+        }
+        lo[q] = pack_e4m3x4(a[0], a[1], a[2], a[3]);
+        hi[q] = pack_e4m3x4(b[0], b[1], b[2], b[3]);
     }
-    uint4* dst = reinterpret_cast<uint4*>(dstT + static_cast<size_t>(c) * n_cols + tile * 128 + k0);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    uint8_t* d0 = dstT + static_cast<size_t>(2 * cp) * n_cols + tile * 128 + k0;
+    *reinterpret_cast<uint4*>(d0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(d0 + n_cols) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    return true;
 }
 
-__global__ void __launch_bounds__(FP8P_THREADS) fp8_prep_kernel(const Fp8PrepParams p, const PlanParams pl) {
+__global__ void __launch_bounds__(FP8P_THREADS, FP8P_BLOCKS_PER_SM)
+    fp8_prep_kernel(const Fp8PrepParams p, const PlanParams pl) {
     grid_dep_launch_dependents();
-    __shared__ uint32_t red[FP8P_THREADS / 32];
-    __shared__ uint16_t vt[128][130];
-    const int tile = blockIdx.x, y = blockIdx.y;
-    const size_t head_elems = static_cast<size_t>(p.N) * 128;
-    if (y < p.heads_q) {
-        fp8_prep_qk_tile(static_cast<const __nv_bfloat16*>(p.Q) + y * head_elems, p.Q8 + y * head_elems,
-                         p.q_exp + static_cast<size_t>(y) * p.n_ktiles + tile, p.signs, p.N, tile, red);
-    } else if (y < p.heads_q + p.heads_kv) {
-        const int h = y - p.heads_q;
-        fp8_prep_qk_tile(static_cast<const __nv_bfloat16*>(p.K) + h * head_elems, p.K8 + h * head_elems,
-                         p.k_exp + static_cast<size_t>(h) * p.n_ktiles + tile, p.signs, p.N, tile, red);
-    } else if (y < p.heads_q + 2 * p.heads_kv) {
-        const int h = y - p.heads_q - p.heads_kv;
-        const int n_cols = p.n_ktiles * 128;
-        fp8_prep_v_tile(static_cast<const __nv_bfloat16*>(p.V) + h * head_elems,
-                        p.V8T + static_cast<size_t>(h) * 128 * n_cols, p.v_exp + static_cast<size_t>(h) * p.n_ktiles + tile,
-                        p.N, n_cols, tile, red, vt);
-    } else if (tile == 0) {
+    extern __shared__ __align__(128) uint8_t fp8p_ring[];
+    __shared__ __align__(8) uint64_t full[FP8P_STAGES];
+    __shared__ uint32_t red[2][FP8P_THREADS / 32];  // block-maximum slots, alternating by tile
+    __shared__ __align__(16) uint16_t vt[128][FP8P_VT_STRIDE];
+    __shared__ __align__(16) uint32_t sgn[4 * 16];  // sign bits of the rotation as bf16-pair XOR masks
+    const int G = static_cast<int>(gridDim.x) - 1;  // tile blocks; the last block plans the schedule
+    if (static_cast<int>(blockIdx.x) == G) {
         plan_block(pl);
+        return;
+    }
+    const int per_y = p.n_ktiles;
+    const int T = per_y * (p.heads_q + 2 * p.heads_kv);  // tiles: Q heads, K heads, V heads (< 2^31)
+    const size_t head_bytes = static_cast<size_t>(p.N) * 256;      // one bf16 [N, 128] slab
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < FP8P_STAGES; ++st) mbar_init(&full[st], 1);
+        fence_mbar_init();
+    }
+    if (p.signs && threadIdx.x < 64) {  // word e of quarter q: elements 32q + 2e (bit 15), + 1 (bit 31)
+        const int el = (threadIdx.x >> 4) * 32 + 2 * (threadIdx.x & 15);
+        sgn[threadIdx.x] = (__ldg(p.signs + el) < 0 ? 0x8000u : 0u) | (__ldg(p.signs + el + 1) < 0 ? 0x80000000u : 0u);
+    }
+    __syncthreads();
+    const uint32_t* sgn_tab = p.signs ? sgn : nullptr;
+    // tile i of the list into ring stage st (one thread)
+    auto issue = [&](int i, int st) {
+        const int y = i / per_y;
+        const int tile = i - y * per_y;
+        const uint8_t* src = y < p.heads_q ? static_cast<const uint8_t*>(p.Q) + static_cast<size_t>(y) * head_bytes
+                           : y < p.heads_q + p.heads_kv
+                               ? static_cast<const uint8_t*>(p.K) + static_cast<size_t>(y - p.heads_q) * head_bytes
+                               : static_cast<const uint8_t*>(p.V) + static_cast<size_t>(y - p.heads_q - p.heads_kv) * head_bytes;
+        const uint32_t bytes = static_cast<uint32_t>(min(128, p.N - tile * 128)) * 256u;
+        mbar_arrive_expect_tx(&full[st], bytes);
+        bulk_load(fp8p_ring + st * FP8P_TILE_BYTES, src + static_cast<size_t>(tile) * 128 * 256, bytes, &full[st]);
+    };
+    if (threadIdx.x == 0)
+        for (int st = 0; st < FP8P_STAGES; ++st) {
+            const int i = static_cast<int>(blockIdx.x) + st * G;
+            if (i < T) issue(i, st);
+        }
+    const size_t head_elems = static_cast<size_t>(p.N) * 128;
+    const int n_cols = p.n_ktiles * 128;
+    volatile int never = 0;
+    int k = 0;
+    bool ok = true;
+    bool prev_v = false;  // the block's previous tile was a V tile (its transposed reads of vt)
+    for (int i = static_cast<int>(blockIdx.x); i < T; i += G, ++k) {
+        const int st = k % FP8P_STAGES;
+        const bool got = mbar_wait(&full[st], (k / FP8P_STAGES) & 1, p.wait_limit_ns, &never);
+        const int y = i / per_y;
+        const int tile = i - y * per_y;
+        const bool is_v = y >= p.heads_q + p.heads_kv;
+        // A V tile overwrites vt, which the previous V tile's threads may still be reading: wait for
+        // them. Otherwise the block maximum's barrier orders the tiles (the reduction slots alternate).
+        // Whether every copy landed is decided block-wide at that barrier.
+        if (is_v && prev_v) __syncthreads();
+        prev_v = is_v;
+        const uint8_t* stage = fp8p_ring + st * FP8P_TILE_BYTES;
+        uint32_t* rd = red[k & 1];
+        // once every thread has read the staged tile, the next tile of the block may land in its stage
+        auto after_max = [&]() {
+            if (threadIdx.x == 0 && i + FP8P_STAGES * G < T) issue(i + FP8P_STAGES * G, st);
+        };
+        if (y < p.heads_q) {
+            ok = fp8_prep_qk_tile(stage, p.Q8 + static_cast<size_t>(y) * head_elems,
+                                  p.q_exp + static_cast<size_t>(y) * per_y + tile, sgn_tab, p.N, tile, rd, !got,
+                                  after_max);
+        } else if (!is_v) {
+            const int h = y - p.heads_q;
+            ok = fp8_prep_qk_tile(stage, p.K8 + static_cast<size_t>(h) * head_elems,
+                                  p.k_exp + static_cast<size_t>(h) * per_y + tile, sgn_tab, p.N, tile, rd, !got,
+                                  after_max);
+        } else {
+            const int h = y - p.heads_q - p.heads_kv;
+            ok = fp8_prep_v_tile(stage, p.V8T + static_cast<size_t>(h) * 128 * n_cols,
+                                 p.v_exp + static_cast<size_t>(h) * per_y + tile, p.N, n_cols, tile, rd, vt, !got,
+                                 after_max);
+        }
+        if (!ok) break;  // block-uniform
+    }
+    if (!ok && threadIdx.x == 0) {
+        // a copy that never landed: record it, then wait (bounded) for the copies still in flight so
+        // that none writes shared memory after the block has exited
+        atomicOr(&g_attn_error, ERRBIT_TIMEOUT | ERRBIT_WAIT_KV);
+        for (int kk = k; kk < k + FP8P_STAGES; ++kk)
+            if (static_cast<int>(blockIdx.x) + kk * G < T)
+                (void)mbar_wait(&full[kk % FP8P_STAGES], (kk / FP8P_STAGES) & 1, p.wait_limit_ns, &never);
     }
 }
 
 cudaError_t launch_fp8_prep(const Fp8PrepParams& p, const PlanParams& plan, cudaStream_t stream) {
-    if (p.d != 128) return cudaErrorInvalidValue;
-    const long long rows = static_cast<long long>(p.heads_q) + 2LL * p.heads_kv + 1;
-    if (rows > 65535) return cudaErrorInvalidConfiguration;
-    fp8_prep_kernel<<<dim3(p.n_ktiles, static_cast<unsigned>(rows)), FP8P_THREADS, 0, stream>>>(p, plan);
+    if (p.d != 128 || p.sms <= 0) return cudaErrorInvalidValue;
+    static std::atomic<int> ready[64];  // once per device: the shared-memory opt-in
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || ready[dev].load(std::memory_order_acquire) == 0) {
+        e = cudaFuncSetAttribute(fp8_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FP8P_SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) ready[dev].store(1, std::memory_order_release);
+    }
+    const long long T = static_cast<long long>(p.n_ktiles) * (p.heads_q + 2LL * p.heads_kv);
+    if (T >= (1LL << 30)) return cudaErrorInvalidConfiguration;  // tile indices stay in int
+    const long long G = std::min<long long>(T, static_cast<long long>(FP8P_BLOCKS_PER_SM) * p.sms);
+    if (G < 1) return cudaErrorInvalidValue;
+    fp8_prep_kernel<<<static_cast<unsigned>(G + 1), FP8P_THREADS, FP8P_SMEM, stream>>>(p, plan);
     return cudaGetLastError();
 }
 
