@@ -323,6 +323,7 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
         p.kv_len = kv_len;
         p.B = B; p.H = H; p.H_kv = H_kv; p.N = N; p.group = H / H_kv; p.causal = causal;
         p.scale = scale;
+        p.wait_limit_ns = g_wait_limit_ns.load();
         return attn_impl::launch_attn_f32(d, p, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     }
 
@@ -517,10 +518,11 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const float* O
 }
 
 attn_status attn_check(cudaStream_t stream) {
-    uint32_t bits = 0, bwd_bits = 0;
+    uint32_t bits = 0, bwd_bits = 0, f32_bits = 0;
     if (attn_impl::read_and_clear_error(&bits, stream) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn_impl::read_and_clear_bwd_error(&bwd_bits) != cudaSuccess) return ATTN_ERR_CUDA;
-    bits |= bwd_bits;
+    if (attn_impl::read_and_clear_f32_error(&f32_bits) != cudaSuccess) return ATTN_ERR_CUDA;
+    bits |= bwd_bits | f32_bits;
     g_last_error_bits.store(bits);
     return bits ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }

@@ -260,6 +260,7 @@ struct F32Params {
     const int32_t* kv_len;
     int B, H, H_kv, N, group, causal;
     float scale;
+    uint64_t wait_limit_ns;   // bound of the wait for the staged key rows
 };
 
 // V (bf16 [heads, N, d]) -> fp16 copy, one 128-row key tile at a time: tile j of head z is stored as
@@ -319,6 +320,7 @@ cudaError_t launch_attn_bwd(int d, const BwdPrepParams& prep, const CUtensorMap&
                             const CUtensorMap& tmV, const CUtensorMap& tmDO, const CUtensorMap& tmDQ,
                             const BwdParams& p, cudaStream_t stream);
 cudaError_t read_and_clear_bwd_error(uint32_t* out);
+cudaError_t read_and_clear_f32_error(uint32_t* out);
 
 // Device error word of the current device: read and clear (synchronous on `stream`).
 cudaError_t read_and_clear_error(uint32_t* out, cudaStream_t stream);
