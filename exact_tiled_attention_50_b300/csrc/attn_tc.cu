@@ -57,32 +57,6 @@ using namespace attn_sm103;
 
 __device__ unsigned int g_attn_error = 0;
 
-// Optional timeline trace (builds with -DATTN_TRACE only): clock64 stamps of CTA 0's MMA warp (per
-// ring step) and of thread 0 of each softmax warpgroup (per key step of its tile), for profiling the
-// pipeline by hand.
-#ifdef ATTN_TRACE
-constexpr int TRACE_J = 128, TRACE_EV = 8;
-__device__ long long g_attn_trace[3][TRACE_J][TRACE_EV];
-#define ATTN_TRACE_AT(role, j, ev)                                                    \
-    do {                                                                             \
-        if (blockIdx.x == 0 && (j) < TRACE_J) g_attn_trace[role][j][ev] = clock64(); \
-    } while (0)
-// per CTA and segment: global-timer stamps (ns) of segment events, for the whole grid
-constexpr int TRACE_CTAS = 160, TRACE_SEGS = 16, TRACE_SEG_EV = 12;
-__device__ long long g_attn_seg_trace[TRACE_CTAS][TRACE_SEGS][TRACE_SEG_EV];
-#define ATTN_SEG_TRACE(seg, ev, val)                                                          \
-    do {                                                                                      \
-        if (blockIdx.x < TRACE_CTAS && (seg) < TRACE_SEGS) g_attn_seg_trace[blockIdx.x][seg][ev] = (val); \
-    } while (0)
-#else
-#define ATTN_SEG_TRACE(seg, ev, val) \
-    do {                             \
-    } while (0)
-#define ATTN_TRACE_AT(role, j, ev) \
-    do {                           \
-    } while (0)
-#endif
-
 namespace {
 
 constexpr int BLOCK_M = 128;              // query rows per tile (tcgen05 M)
@@ -450,19 +424,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t g = 0, segq = 0;    // ring steps consumed, segments with a Q load
             uint32_t cnt_p[2] = {0u, 0u};
             bool ok = true;
-            int seg_no = -1;  // trace index
             while (ok && next_seg()) {
-                ++seg_no;
                 const SegInfo si = seg_info(p, s);
-                if (lane == 0) ATTN_SEG_TRACE(seg_no, 0, static_cast<long long>(global_timer_ns()));
-                if (lane == 0) ATTN_SEG_TRACE(seg_no, 6, s.kind * 1000000LL + (s.k1 - s.k0));
                 if (si.nmax == 0) continue;
                 if (!wait_all(&bar_k0_full, segq & 1, ERRBIT_WAIT_KV) || !wait_all(&bar_q, segq & 1, ERRBIT_WAIT_Q)) {
                     ok = false;
                     break;
                 }
                 ++segq;
-                if (lane == 0) ATTN_SEG_TRACE(seg_no, 1, static_cast<long long>(global_timer_ns()));
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
@@ -476,13 +445,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 for (int jj = 0; jj < si.nmax; ++jj) {
                     const uint32_t st = g % C::NP;
-                    ATTN_TRACE_AT(0, g, 4);
                     if (!wait_all(&bar_full[st], (g / C::NP) & 1, ERRBIT_WAIT_KV)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    ATTN_TRACE_AT(0, g, 5);
                     const uint64_t dv = dRingV + static_cast<uint64_t>((st * C::STAGE_BYTES) >> 4);
                     const uint64_t dk = dRingK + static_cast<uint64_t>((st * C::STAGE_BYTES) >> 4);
 #pragma unroll
@@ -493,7 +460,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             continue;
                         }
                         tc_fence_after();
-                        ATTN_TRACE_AT(0, g, 2 * t);
                         if (elect_one()) issue_PV_half(t, dv, 0, jj > 0);
                         __syncwarp();
                         if (!wait_all(&bar_p_full[t][1], cnt_p[t] & 1, ERRBIT_WAIT_P)) {
@@ -512,7 +478,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                         }
                         __syncwarp();
-                        ATTN_TRACE_AT(0, g, 2 * t + 1);
                     }
                     if (!ok) break;
                     if (elect_one()) umma_commit(&bar_empty[st]);
@@ -523,7 +488,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // Q of this segment may be overwritten once these MMAs completed
                 if (elect_one()) umma_commit(&bar_q_empty);
                 __syncwarp();
-                if (lane == 0) ATTN_SEG_TRACE(seg_no, 2, static_cast<long long>(global_timer_ns()));
             }
             // Drain: every MMA this warp issued has completed before tensor memory is freed.
             if (elect_one()) umma_commit(&bar_drain);
@@ -543,16 +507,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t tS = tmem + lane_off + t * BLOCK_N;
         const uint32_t tO = tmem + lane_off + C::TMEM_O + t * D;
         const float sl = p.scale_log2;
-        const bool trace_me = (threadIdx.x & 127) == 0;
         const int G = p.plan.G;
         const Segment& s = seg_sh[warp];
-        uint32_t cnt_s = 0, cnt_o = 0;  // cnt_s also numbers this tile's key steps (trace index)
+        uint32_t cnt_s = 0, cnt_o = 0;  // S_t and O_t phases waited for
         uint32_t segq = 0;              // segments whose Q the producer loaded (as it counts them)
         bool ok = true;
-        int seg_no = -1;  // trace index
 
         while (ok && next_seg()) {
-            ++seg_no;
             // In a segment whose Q the producer loads, this warpgroup may hand Q_t's shared memory
             // back (bar_q_free) only after that load landed: the producer then waits for exactly one
             // outstanding q_free phase per tile, even for a tile without keys in the segment.
@@ -643,7 +604,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 // tcgen05.ld/st below are warp-collective: the warp proceeds only if every lane's wait
                 // succeeded
-                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s, 0);
                 const bool got = mbar_wait(&bar_s_full[t], cnt_s & 1, limit_ns, &abort_flag);
                 ++cnt_s;
                 if (!__all_sync(0xffffffffu, got)) {
@@ -652,7 +612,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 1);
                 float x[128];
                 if constexpr (EXTRA) {
                     // scores to the log2 domain with the bias added: x = S * scale*log2e + bias * log2e,
@@ -699,7 +658,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         x[96 + i] = __uint_as_float(rd[i]);
                     }
                 }
-                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 2);
                 const int key0 = j * BLOCK_N;
                 if (key0 + BLOCK_N > kv_valid || (p.plan.causal && key0 + BLOCK_N - 1 > q0t)) {
                     const int lim = row_lim - key0;
@@ -759,7 +717,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tmem_st32(tO + c * 32, o);
                     }
                 }
-                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 3);
                 const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
                 // P = exp2(s * scale*log2e - m), written to TMEM as fp16 pairs over the first 64 columns
                 // of S_t, one half (64 keys) at a time; each half is announced as soon as it is stored.
@@ -828,7 +785,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tmem_wait_st();
                         tc_fence_before();
                         mbar_arrive(&bar_p_full[t][half]);
-                        if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 4 + half);
                     }
                     float s0, s1, s2, s3;
                     split_f32x2(acc0, s0, s1);
@@ -836,7 +792,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const float psum = (s0 + s1) + (s2 + s3);
                     l_run += shift == 0 ? psum : ldexpf(psum, -shift);
                 }
-                if (trace_me) ATTN_TRACE_AT(1 + t, cnt_s - 1, 6);
             }
             if (!ok) break;
 
@@ -855,7 +810,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool live = have && l_run > 0.f;     // this row got weight from this piece
             // the producer loads Q (and waits for this warpgroup's q_free) only for segments with keys
             const bool seg_loads_q = seg_info(p, s).nmax > 0;
-            if ((threadIdx.x & 127) == 0) ATTN_SEG_TRACE(seg_no, 3 + t, static_cast<long long>(global_timer_ns()));
 
             if (s.kind == SEG_WRITER) {
                 // partial result for the owner of the unit: unnormalised O (row fastest), m, l
@@ -927,7 +881,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
             }
-            if (t == 0 && r == 0) ATTN_SEG_TRACE(seg_no, 8, static_cast<long long>(global_timer_ns()));
             // softmax merge of the pieces: weights 2^(m_i - M) on l, 2^(m_i - M + E_i - Emax) on O
             const float w_own_l = live ? ex2_approx(m_run - M) : 0.f;
             const float w_own = live ? w_own_l * pow2i(E - Emax) : 0.f;
@@ -953,7 +906,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (l2 > 0.f) L += ex2_approx(__ldcg(b2 + D * BLOCK_M + r) - M) * l2;
                 }
             }
-            if (t == 0 && r == 0) ATTN_SEG_TRACE(seg_no, 9, static_cast<long long>(global_timer_ns()));
             const int bh = s.b * p.plan.H + s.h;
             float inv = L > 0.f ? pow2i(Emax) * __frcp_rn(L) : 0.f;
             if constexpr (EXTRA) inv *= p.keep_scale;  // inverted dropout (1 without dropout)
@@ -1093,12 +1045,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float lse = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
                 p.LSE[static_cast<size_t>(bh) * p.plan.N + row] = lse;
             }
-            if (t == 0 && r == 0) ATTN_SEG_TRACE(seg_no, 10, static_cast<long long>(global_timer_ns()));
             if (lane == 0 && seg_loads_q) {
                 if (!OUT_BF16) bulk_wait_group_read<0>();  // the staging buffers may be overwritten
                 mbar_arrive(&bar_q_free[t]);
             }
-            if ((threadIdx.x & 127) == 0) ATTN_SEG_TRACE(seg_no, 5 + 2 * t, static_cast<long long>(global_timer_ns()));
         }
     }
 
@@ -1624,18 +1574,6 @@ cudaError_t launch_attn_tc_fp8(const CUtensorMap& tmQ8, const CUtensorMap& tmK8,
                                const CUtensorMap& tmO, const TcParams& p, cudaStream_t stream) {
     return launch_tc_t<128, false, 1>(tmQ8, tmK8, tmVT8, tmO, p, stream);
 }
-
-#ifdef ATTN_TRACE
-extern "C" int attn_debug_read_trace(long long* host, int n) {
-    if (n < 3 * TRACE_J * TRACE_EV) return -1;
-    return cudaMemcpyFromSymbol(host, g_attn_trace, sizeof(g_attn_trace)) == cudaSuccess ? 0 : -1;
-}
-
-extern "C" int attn_debug_read_seg_trace(long long* host, int n) {
-    if (n < TRACE_CTAS * TRACE_SEGS * TRACE_SEG_EV) return -1;
-    return cudaMemcpyFromSymbol(host, g_attn_seg_trace, sizeof(g_attn_seg_trace)) == cudaSuccess ? 0 : -1;
-}
-#endif
 
 // Line length of the worst case (every kv_len = N): the schedule needs it below 2^31.
 long long plan_max_steps(int B, int H, int N, int causal) {
