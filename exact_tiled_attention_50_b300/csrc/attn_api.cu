@@ -560,7 +560,7 @@ int attn_debug_schedule(int B, int H, int N, int causal, const int32_t* kv_len_h
         int L = kv_len_host ? kv_len_host[b] : N;
         L = L < 0 ? 0 : (L > N ? N : L);
         nb[b] = attn_impl::key_tiles(L);
-        boff[b + 1] = boff[b] + static_cast<long long>(H) * attn_impl::pair_prefix(plan.n_pairs, nb[b], N, plan.causal);
+        boff[b + 1] = boff[b] + static_cast<long long>(H) * attn_impl::line_prefix(plan.n_pairs, nb[b], N, plan.causal);
     }
     const attn_impl::HostSchedTab tab{nb.data(), boff.data()};
     int n = 0;

@@ -26,11 +26,15 @@ enum : uint32_t {
 // A work unit is (b, h, pair): 256 query rows (two 128-row query tiles) of one head. Its cost is the
 // number of 128-key steps it needs: the larger of its two tiles' key-tile counts below
 // min(kv_len[b], causal limit), and at least 1 (a unit without any valid key still writes O = 0,
-// LSE = -inf). Units lie on a line in (b, h, pair) order; unit u covers [off(u), off(u) + cost(u)).
-// CTA c of G first runs R_dp data-parallel rounds (unit r*G + c in round r, while that unit exists),
-// then, when the plan has a stream-K part (sk = 1), one contiguous chunk of the rest of the line,
-// [S0 + (W - S0) c / G, S0 + (W - S0) (c + 1) / G). A unit that a chunk boundary cuts is computed in
-// pieces over disjoint key ranges. The piece that holds the unit's first key step (the owner) is the
+// LSE = -inf). Units lie on a line in (b, h, pair) order; unit u covers [off(u), off(u) + OVH +
+// cost(u)): OVH = SCHED_UNIT_OVERHEAD positions stand for the fixed time of a segment (its Q load,
+// first S and epilogue), then one position per key step. CTA c of G first runs R_dp data-parallel
+// rounds (unit r*G + c in round r, while that unit exists), then, when the plan has a stream-K part
+// (sk = 1), one contiguous chunk of the rest of the line, [S0 + (W - S0) c / G, S0 + (W - S0) (c + 1) /
+// G): equal chunks of the line give every CTA the same key steps plus segment overheads, so a CTA
+// with many short units gets fewer steps. A chunk boundary inside a unit's overhead belongs to the
+// unit's start (the unit goes whole to the later chunk); a unit that a boundary cuts inside its key
+// steps is computed in pieces over disjoint key ranges. The piece that holds the unit's first key step (the owner) is the
 // last segment of its CTA; the other pieces are the first segments of the following CTAs' chunks,
 // which write their partial results (unnormalised O, running max m, running sum l) to a slot of
 // their own. The owner merges them with the softmax merge rule: m = max(m_a, m_b),
@@ -44,6 +48,9 @@ constexpr int SCHED_MIN_STEPS = 2;   // the CTA count is capped so that chunks h
 // lost by 6-10 steps' worth on small problems and won by about 30 steps at N = 8192; the plan splits
 // units only when that saves more than this.
 constexpr int SCHED_SPLIT_PENALTY = 10;
+// Line positions per unit before its key steps: a segment's fixed time (Q load, first S, epilogue and
+// the next segment's start) measured at about two key steps' worth on B300 (B1 H16 N8192 d128).
+constexpr int SCHED_UNIT_OVERHEAD = 2;
 
 enum : int { SEG_COMPLETE = 0, SEG_OWNER = 1, SEG_WRITER = 2 };
 
@@ -64,6 +71,11 @@ __host__ __device__ inline long long pair_prefix(int P, int nb, int N, int causa
 
 __host__ __device__ inline int pair_cost(int pair, int nb, int N, int causal) {
     return static_cast<int>(pair_prefix(pair + 1, nb, N, causal) - pair_prefix(pair, nb, N, causal));
+}
+
+// Line length of pairs [0, P) of one head: their key steps and the overhead of each unit.
+__host__ __device__ inline long long line_prefix(int P, int nb, int N, int causal) {
+    return pair_prefix(P, nb, N, causal) + static_cast<long long>(SCHED_UNIT_OVERHEAD) * P;
 }
 
 struct SchedPlan {
@@ -108,7 +120,7 @@ __host__ __device__ inline void walk_init(WalkState& w, const Tab& t, const Sche
 
 template <class Tab>
 __host__ __device__ inline int walk_head_cost(const Tab& t, const SchedPlan& p, int b) {
-    return static_cast<int>(pair_prefix(p.n_pairs, t.nb(b), p.N, p.causal));
+    return static_cast<int>(line_prefix(p.n_pairs, t.nb(b), p.N, p.causal));
 }
 
 // b, h, pair and unit_off of the unit that contains line position x (boff(0) <= x < W)
@@ -127,13 +139,13 @@ __host__ __device__ inline void walk_locate(WalkState& w, const Tab& t, const Sc
     w.h = rem / hc;
     const int r2 = rem - w.h * hc;
     int plo = 0, phi = p.n_pairs - 1;
-    while (plo < phi) {  // largest pair with pair_prefix(pair) <= r2
+    while (plo < phi) {  // largest pair with line_prefix(pair) <= r2
         const int mid = (plo + phi + 1) / 2;
-        if (pair_prefix(mid, nb, p.N, p.causal) <= r2) plo = mid;
+        if (line_prefix(mid, nb, p.N, p.causal) <= r2) plo = mid;
         else phi = mid - 1;
     }
     w.pair = plo;
-    w.unit_off = static_cast<int>(t.boff(lo)) + w.h * hc + static_cast<int>(pair_prefix(plo, nb, p.N, p.causal));
+    w.unit_off = static_cast<int>(t.boff(lo)) + w.h * hc + static_cast<int>(line_prefix(plo, nb, p.N, p.causal));
 }
 
 template <class Tab>
@@ -166,16 +178,19 @@ __host__ __device__ inline bool walk_next(WalkState& w, const Tab& t, const Sche
     }
     if (w.pos >= w.chunk_end) return false;
     const int cost = pair_cost(w.pair, t.nb(w.b), p.N, p.causal);
-    const int end = w.unit_off + cost;
+    const int step0 = w.unit_off + SCHED_UNIT_OVERHEAD;  // line position of the unit's first key step
+    const int end = step0 + cost;
+    const int k1 = (w.chunk_end < end ? w.chunk_end : end) - step0;
+    if (k1 <= 0) return false;  // the chunk ends inside this unit's overhead: the next chunk takes it
     s.b = w.b;
     s.h = w.h;
     s.pair = w.pair;
     s.cost = cost;
-    s.k0 = w.pos - w.unit_off;
-    s.k1 = (w.chunk_end < end ? w.chunk_end : end) - w.unit_off;
+    s.k0 = w.pos > step0 ? w.pos - step0 : 0;
+    s.k1 = k1;
     s.unit_end = end;
     s.kind = s.k0 > 0 ? SEG_WRITER : (s.k1 < cost ? SEG_OWNER : SEG_COMPLETE);
-    w.pos = w.unit_off + s.k1;
+    w.pos = step0 + k1;
     w.unit_off = end;
     if (++w.pair == p.n_pairs) {
         w.pair = 0;

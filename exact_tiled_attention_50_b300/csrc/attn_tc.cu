@@ -146,7 +146,7 @@ struct DevSchedTab {
     __device__ long long boff(int b) const {
         if (p.kv_len == nullptr)
             return static_cast<long long>(b) * p.plan.H *
-                   pair_prefix(p.plan.n_pairs, key_tiles(p.plan.N), p.plan.N, p.plan.causal);
+                   line_prefix(p.plan.n_pairs, key_tiles(p.plan.N), p.plan.N, p.plan.causal);
         return p.boff[b];
     }
 };
@@ -1067,7 +1067,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // |V| maximum and the conversion). The tile's exponent e keeps |V| * 2^-e < 2^15; values too small
 // for fp16 lose only absolute precision far below the result's rounding (below 2^-25 |V|max).
 // ---------------------------------------------------------------------------------------------
-// The schedule's batch offsets: boff[b] = sum over b' < b of H * (one head's cost in batch b'),
+// The schedule's batch offsets: boff[b] = sum over b' < b of H * (one head's line length in batch b'),
 // computed by one block; it also clears the partial-result flags of the attention kernel.
 __device__ void plan_block(const PlanParams& pl) {
     __shared__ long long part[256];
@@ -1078,7 +1078,7 @@ __device__ void plan_block(const PlanParams& pl) {
     long long sum = 0;
     for (int b = b0; b < b1; ++b) {
         const int nb = key_tiles(clamp_len(pl.kv_len, b, pl.N));
-        sum += static_cast<long long>(pl.H) * pair_prefix(pl.n_pairs, nb, pl.N, pl.causal);
+        sum += static_cast<long long>(pl.H) * line_prefix(pl.n_pairs, nb, pl.N, pl.causal);
     }
     if (act) part[tid] = sum;
     __syncthreads();
@@ -1096,7 +1096,7 @@ __device__ void plan_block(const PlanParams& pl) {
     for (int b = b0; b < b1; ++b) {
         pl.boff[b] = run;
         const int nb = key_tiles(clamp_len(pl.kv_len, b, pl.N));
-        run += static_cast<long long>(pl.H) * pair_prefix(pl.n_pairs, nb, pl.N, pl.causal);
+        run += static_cast<long long>(pl.H) * line_prefix(pl.n_pairs, nb, pl.N, pl.causal);
     }
     for (int i = tid; i < 8 * SCHED_MAX_CTAS; i += blockDim.x) pl.flags[i] = 0u;
 }
@@ -1578,7 +1578,7 @@ cudaError_t launch_attn_tc_fp8(const CUtensorMap& tmQ8, const CUtensorMap& tmK8,
 // Line length of the worst case (every kv_len = N): the schedule needs it below 2^31.
 long long plan_max_steps(int B, int H, int N, int causal) {
     const int n_pairs = (N + 2 * BLOCK_M - 1) / (2 * BLOCK_M);
-    return static_cast<long long>(B) * H * pair_prefix(n_pairs, key_tiles(N), N, causal);
+    return static_cast<long long>(B) * H * line_prefix(n_pairs, key_tiles(N), N, causal);
 }
 
 SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms, int mode) {
@@ -1591,10 +1591,11 @@ SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms, i
     const long long units = static_cast<long long>(B) * H * p.n_pairs;
     p.units = static_cast<int>(units);
     const int nb = key_tiles(N);
-    const long long w_max = static_cast<long long>(B) * H * pair_prefix(p.n_pairs, nb, N, causal);
+    const long long w_max = static_cast<long long>(B) * H * line_prefix(p.n_pairs, nb, N, causal);
     const long long g_cap = sms < SCHED_MAX_CTAS ? sms : SCHED_MAX_CTAS;
-    // Two plans, compared by the key steps of the busiest CTA (kv_len counts as N: an upper bound).
-    // Stream-K: G CTAs share the line evenly, units cut by chunk boundaries pay the merge penalty.
+    // Two plans, compared by the key steps plus unit overheads of the busiest CTA (kv_len counts as N:
+    // an upper bound). Stream-K: G CTAs share the line evenly, units cut by chunk boundaries pay the
+    // merge penalty.
     long long g = g_cap;
     const long long g_steps = (w_max + SCHED_MIN_STEPS - 1) / SCHED_MIN_STEPS;
     if (g_steps < g) g = g_steps;
@@ -1610,7 +1611,8 @@ SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms, i
         if (c > max_cost) max_cost = c;
     }
     const long long rounds = (units + g_cap - 1) / g_cap;
-    const long long t_whole = uniform ? rounds * nb : (rounds == 1 ? max_cost : -1);
+    const long long t_whole =
+        uniform ? rounds * (nb + SCHED_UNIT_OVERHEAD) : (rounds == 1 ? max_cost + SCHED_UNIT_OVERHEAD : -1);
     if (mode == 1 || (mode == 0 && t_whole >= 0 && t_whole < t_stream)) {
         p.R_dp = static_cast<int>(rounds);
         p.G = static_cast<int>((units + rounds - 1) / rounds);  // the fewest CTAs for that many rounds
@@ -1624,7 +1626,7 @@ SchedPlan make_plan(int B, int H, int N, int causal, bool has_kv_len, int sms, i
     // units go to the balanced stream-K part
     const long long r = uniform ? units / g - 1 : 0;
     p.R_dp = r > 0 ? static_cast<int>(r) : 0;
-    p.S0 = static_cast<int>(static_cast<long long>(p.R_dp) * p.G * nb);
+    p.S0 = static_cast<int>(static_cast<long long>(p.R_dp) * p.G * (nb + SCHED_UNIT_OVERHEAD));
     return p;
 }
 

@@ -83,6 +83,7 @@ def test_schedule_covers_every_key_step_once(attn, B, H, N, causal, kv_len, sms)
 
 
 SPLIT_PENALTY = 10  # key steps a stream-K plan costs beyond its even share (the plan's cost model)
+UNIT_OVERHEAD = 2   # line positions of a unit before its key steps (a segment's fixed time)
 
 
 def plan_kind(segs):
@@ -104,13 +105,16 @@ def test_schedule_roles_and_balance(attn, B, H, N, causal, kv_len, sms):
         if WRITER in kinds:
             assert all(k == COMPLETE for k in kinds[:kinds.index(WRITER)])
         assert kinds.count(OWNER) <= 1 and (OWNER not in kinds or kinds[-1] == OWNER)
-        load.append(sum(s[5] - s[4] for s in lst))
+        # key steps plus the overhead of every unit the CTA starts (a writer piece starts none)
+        load.append(sum(s[5] - s[4] + (UNIT_OVERHEAD if s[4] == 0 else 0) for s in lst))
     assert min(load) >= 1  # no CTA is launched without work
     n_pairs = math.ceil(N / 256)
     units = B * H * n_pairs
     if plan_kind(segs) == "stream":
-        # every CTA gets the mean load up to rounding (whole data-parallel units weigh the same)
-        assert max(load) - min(load) <= 1, (min(load), max(load), sum(load) / G)
+        # every CTA gets an equal chunk of the line up to rounding; a chunk boundary inside (or at the
+        # end of) a unit's overhead moves that overhead to the CTA that starts the unit: at most
+        # UNIT_OVERHEAD more on one CTA and as much less on the one before it
+        assert max(load) - min(load) <= 1 + 2 * UNIT_OVERHEAD, (min(load), max(load), sum(load) / G)
     else:
         # whole units in rounds: unit r * G + c on CTA c, no CTA idle in the first round
         assert G == math.ceil(units / math.ceil(units / G))
@@ -120,18 +124,19 @@ def test_schedule_roles_and_balance(attn, B, H, N, causal, kv_len, sms):
 
 
 def model_makespans(B, H, N, causal, padded, sms):
-    """Busiest CTA's key steps under each plan (kv_len counted as N), as the plan's cost model states."""
+    """Busiest CTA's key steps plus unit overheads under each plan (kv_len counted as N), as the
+    plan's cost model states."""
     nb = math.ceil(N / 128)
     n_pairs = math.ceil(N / 256)
     costs = [unit_cost(N, causal, N, p) for p in range(n_pairs)]
-    w = B * H * sum(costs)
+    w = B * H * (sum(costs) + UNIT_OVERHEAD * n_pairs)
     g_cap = min(sms, 160)
     g = max(1, min(g_cap, math.ceil(w / 2)))
     t_stream = math.ceil(w / g) + SPLIT_PENALTY
     units = B * H * n_pairs
     rounds = math.ceil(units / g_cap)
     uniform = not causal and not padded
-    t_whole = rounds * nb if uniform else (max(costs) if rounds == 1 else None)
+    t_whole = rounds * (nb + UNIT_OVERHEAD) if uniform else (max(costs) + UNIT_OVERHEAD if rounds == 1 else None)
     return t_whole, t_stream
 
 
