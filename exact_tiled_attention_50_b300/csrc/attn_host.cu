@@ -51,22 +51,43 @@ Pipe* pipe_for_current_device() {
 
 size_t elem_bytes(attn_dtype t) { return t == ATTN_F32 ? 4 : 2; }
 
-// Key/value heads per group for these sizes: groups never span two batches; per batch,
-// ceil(want / B) ranges of key/value heads.
-int heads_per_group(int B, int H_kv, int n_groups) {
+// Groups of key/value heads per batch for these sizes: about `n_groups` in all (8 by default, at most
+// 64 over every batch), never spanning two batches. With three or more per batch the first and the
+// last group are half the size of the others: the first group's copy in and the last group's copy
+// back are the parts of the pipeline that nothing overlaps. 0 when even one group per batch exceeds 64.
+int groups_per_batch(int B, int H_kv, int n_groups) {
     long long want = n_groups > 0 ? n_groups : 8;
     if (want > kMaxGroups) want = kMaxGroups;
-    const long long per_batch = (want + B - 1) / B;
-    return static_cast<int>((H_kv + per_batch - 1) / per_batch);
+    long long per = (want + B - 1) / B;
+    if (per >= 2) ++per;  // two half-size groups at the ends take the place of one
+    if (per > H_kv) per = H_kv;
+    if (per * B > kMaxGroups) per = kMaxGroups / B;
+    return static_cast<int>(per);
+}
+
+// First key/value head of group i (0 <= i <= n) of a batch whose H_kv heads form n groups (n <= H_kv):
+// weights 1, 2, ..., 2, 1 for n >= 3 (equal otherwise), boundaries rounded, every group kept non-empty.
+int group_start(int H_kv, int n, int i) {
+    if (i <= 0) return 0;
+    if (i >= n) return H_kv;
+    long long h;
+    if (n < 3) {
+        h = static_cast<long long>(H_kv) * i / n;
+    } else {
+        const long long W = 2LL * n - 2;
+        h = (static_cast<long long>(H_kv) * (2LL * i - 1) + W / 2) / W;
+    }
+    if (h < i) h = i;                      // room for the i groups before
+    if (h > H_kv - (n - i)) h = H_kv - (n - i);  // and for the n - i after
+    return static_cast<int>(h);
 }
 
 }  // namespace
 
 extern "C" int attn_fwd_host_groups(int B, int H_kv, int n_groups) {
     if (B <= 0 || H_kv <= 0) return -1;
-    const int ck = heads_per_group(B, H_kv, n_groups);
-    const long long groups = static_cast<long long>(B) * ((H_kv + ck - 1) / ck);
-    return groups <= kMaxGroups ? static_cast<int>(groups) : -1;
+    const int per = groups_per_batch(B, H_kv, n_groups);
+    return per > 0 ? B * per : -1;
 }
 
 extern "C" attn_status attn_fwd_host(const void* Q_h, const void* K_h, const void* V_h, void* O_h, float* LSE_h,
@@ -80,10 +101,15 @@ extern "C" attn_status attn_fwd_host(const void* Q_h, const void* K_h, const voi
     if (B <= 0 || H <= 0 || H_kv <= 0 || N <= 0 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
     if ((in_dtype != ATTN_F32 && in_dtype != ATTN_BF16) || (out_dtype != ATTN_F32 && out_dtype != ATTN_BF16))
         return ATTN_ERR_INVALID_ARG;
-    if (attn_fwd_host_groups(B, H_kv, n_groups) <= 0) return ATTN_ERR_UNSUPPORTED;  // more than 64 groups
-    const int ck = heads_per_group(B, H_kv, n_groups);
+    const int n_per = groups_per_batch(B, H_kv, n_groups);
+    if (n_per <= 0) return ATTN_ERR_UNSUPPORTED;  // more than 64 groups
     const int g = H / H_kv;
-    // every group's call needs at most the workspace of the whole problem; check it once here
+    int ck = 0;  // key/value heads of the largest group
+    for (int i = 0; i < n_per; ++i) {
+        const int nk = group_start(H_kv, n_per, i + 1) - group_start(H_kv, n_per, i);
+        if (nk > ck) ck = nk;
+    }
+    // the largest group's call needs the most workspace (the whole problem's is always enough)
     if (in_dtype == ATTN_BF16 && workspace_bytes < attn_workspace_bytes(1, ck * g, ck, N, d, in_dtype))
         return ATTN_ERR_INVALID_ARG;
     Pipe* pp = pipe_for_current_device();
@@ -100,8 +126,9 @@ extern "C" attn_status attn_fwd_host(const void* Q_h, const void* K_h, const voi
         return ATTN_ERR_CUDA;
     int k = 0;
     for (int b = 0; b < B; ++b) {
-        for (int h0 = 0; h0 < H_kv; h0 += ck, ++k) {
-            const int nk = h0 + ck <= H_kv ? ck : H_kv - h0;  // key/value heads of this group
+        for (int i = 0; i < n_per; ++i, ++k) {
+            const int h0 = group_start(H_kv, n_per, i);
+            const int nk = group_start(H_kv, n_per, i + 1) - h0;  // key/value heads of this group
             const size_t zq = static_cast<size_t>(b) * H + static_cast<size_t>(h0) * g;  // first query head
             const size_t zk = static_cast<size_t>(b) * H_kv + h0;                          // first key/value head
             const size_t nq_el = static_cast<size_t>(nk) * g * head, nk_el = static_cast<size_t>(nk) * head;

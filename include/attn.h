@@ -184,7 +184,9 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const float* O
  *   workspace    device, at least attn_workspace_bytes() of one group (the whole problem's size is
  *                always enough), 256-byte aligned, as for attn_fwd
  *   n_groups     head groups to aim for (0: 8); never more than 64, and a group never spans two
- *                batches: attn_fwd_host_groups() gives the number the call will use
+ *                batches; with two or more groups per batch the batch gets one more, the first and
+ *                the last half the size of the others (their copies are the ones nothing overlaps):
+ *                attn_fwd_host_groups() gives the number the call will use
  *   stream       the call's stream: the inputs are read after the work already on it, the kernels run
  *                on it, and it reaches the end of the call once every output is back in host memory
  *                (the copies run on two streams the library creates per device on first use and keeps)

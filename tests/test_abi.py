@@ -129,3 +129,30 @@ def _call_ex(lib, **kw):
 ])
 def test_ex_invalid_arguments_rejected_without_launch(lib, bad):
     assert _call_ex(lib, **bad) == lib.ATTN_ERR_INVALID_ARG
+
+
+def _groups_per_batch(B, H_kv, n_groups):
+    """The host pipeline's groups per batch, restated: about n_groups in all (8 by default, at most
+    64), one more per batch when there are at least two (half-size groups at both ends), at most one
+    per key/value head, and at most 64 over every batch (0: unsupported)."""
+    per = -(-min(n_groups if n_groups > 0 else 8, 64) // B)
+    if per >= 2:
+        per += 1
+    per = min(per, H_kv)
+    if per * B > 64:
+        per = 64 // B
+    return per
+
+
+@pytest.mark.parametrize("B,H_kv,n_groups", [
+    (1, 16, 0), (1, 16, 3), (2, 2, 0), (2, 1, 64), (8, 16, 64), (64, 1, 0), (65, 1, 0), (3, 5, 7), (1, 1, 0),
+    (4, 32, 16), (33, 4, 64),
+])
+def test_host_pipeline_group_count(lib, B, H_kv, n_groups):
+    per = _groups_per_batch(B, H_kv, n_groups)
+    assert lib.lib.attn_fwd_host_groups(B, H_kv, n_groups) == (B * per if per > 0 else -1)
+
+
+def test_host_pipeline_invalid_sizes(lib):
+    assert lib.lib.attn_fwd_host_groups(0, 4, 0) == -1
+    assert lib.lib.attn_fwd_host_groups(2, 0, 0) == -1

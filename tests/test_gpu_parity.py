@@ -248,7 +248,7 @@ def test_both_work_plans_match_the_oracle(mode, causal):
 # ---------------------------------------------------------------- host buffers, pipelined over head groups
 @pytest.mark.parametrize("B,H,H_kv,N,d,dtype,causal,padded,n_groups", [
     (2, 8, 2, 600, 128, "bf16", True, True, 0),     # 2 batches x 2 kv heads: 4 groups
-    (1, 16, 16, 384, 64, "bf16", False, False, 3),  # uneven groups (6, 6, 4 kv heads)
+    (1, 16, 16, 384, 64, "bf16", False, False, 3),  # tapered groups (3, 5, 5, 3 kv heads)
     (2, 4, 1, 300, 128, "bf16", True, False, 64),   # MQA: one group per batch
     (1, 2, 2, 256, 64, "f32", False, False, 0),
 ])
