@@ -81,8 +81,10 @@ struct Cfg {
     static constexpr int BOX_ELEMS = FP8 ? 128 : 64;  // elements per 128-byte box row
     static constexpr int NB = D / BOX_ELEMS;          // boxes per tile row
     static constexpr int TILE_BYTES = NB * 16384;     // one 128 x D tile (fp8: also the 128 x 128 V^T tile)
-    // Shared memory: Q_0, Q_1, the segment's first key tile K_k0, then NP ring stages of
-    // (V_j, K_j+1), consumed together (one wait and one release per key step).
+    // Shared memory: Q_0, Q_1, then NP ring stages of (V_j, K_j+1), consumed together (one wait and one
+    // release per key step; a segment's first stage holds only its first key tile K_k0), then the
+    // epilogue's staging boxes (EPI_BUFS of 4 KB per softmax warp). With staging of its own the
+    // epilogue leaves Q free, so the next segment's Q loads as soon as this segment's MMAs are done.
     static constexpr int NP = (D == 128 && !FP8) ? 2 : 4;
     // S = Q K^T k-steps: 16 bf16 or 32 E4M3 elements, 32 bytes of each row either way
     static constexpr int KSTEPS = FP8 ? D / 32 : D / 16;
@@ -90,19 +92,19 @@ struct Cfg {
     // this (log2 units); exponentials then stay <= 2^15, inside the fp16 range of P (65504), or
     // <= 2^8, inside the E4M3 range (448).
     static constexpr float RESCALE_THRESHOLD = FP8 ? 8.0f : 15.0f;
-    static constexpr int OFF_K0 = 2 * TILE_BYTES;
-    static constexpr int OFF_RING = 3 * TILE_BYTES;
+    static constexpr int OFF_RING = 2 * TILE_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // V slot then K slot
-    static constexpr int SMEM_BYTES = 1024 + OFF_RING + NP * STAGE_BYTES;
+    static constexpr int OFF_EPI = OFF_RING + NP * STAGE_BYTES;
+    // two staging boxes per warp where they fit in the 227 KB a CTA may use, else one
+    static constexpr int EPI_BUFS = 1024 + OFF_EPI + 8 * 2 * 4096 <= 232448 ? 2 : 1;
+    static constexpr int SMEM_BYTES = 1024 + OFF_EPI + 8 * EPI_BUFS * 4096;
     // bf16 S: K-major both; f16 P V: B (V) MN-major. fp8: E4M3 everywhere, every operand K-major
     // (V^T tile: d rows of 128 keys).
     static constexpr uint32_t IDESC_S = FP8 ? idesc_f8f6f4(BLOCK_M, BLOCK_N, 0, 0, 0, 0)
                                             : idesc_f16(BLOCK_M, BLOCK_N, 1, 1, 0, 0);
     static constexpr uint32_t IDESC_O = FP8 ? idesc_f8f6f4(BLOCK_M, D, 0, 0, 0, 0) : idesc_f16(BLOCK_M, D, 0, 0, 0, 1);
     static constexpr uint32_t TMEM_O = 256;
-    // epilogue staging buffers (4 KB each) per softmax warp inside its tile's Q region
-    static constexpr int EPI_BUFS = TILE_BYTES / 4 / 4096;
-    static_assert(EPI_BUFS >= 1, "staging");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 __device__ __forceinline__ void record_failure(volatile int* abort_flag, uint32_t bits) {
@@ -194,14 +196,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     __shared__ __align__(8) uint64_t bar_q;                 // the segment's Q_0, Q_1 landed
     __shared__ __align__(8) uint64_t bar_q_empty;           // every MMA of the segment completed
-    __shared__ __align__(8) uint64_t bar_k0_full;           // the segment's first K tile landed
-    __shared__ __align__(8) uint64_t bar_k0_empty;          // the segment's first S MMAs completed
     __shared__ __align__(8) uint64_t bar_full[C::NP];       // ring stage (V_j, K_j+1) landed
     __shared__ __align__(8) uint64_t bar_empty[C::NP];      // ring stage free again
     __shared__ __align__(8) uint64_t bar_s_full[2];         // S_t in TMEM
     __shared__ __align__(8) uint64_t bar_p_full[2][2];      // half h of P_t in TMEM (O_t rescaled)
     __shared__ __align__(8) uint64_t bar_o_full[2];         // last P V of the segment into O_t done
-    __shared__ __align__(8) uint64_t bar_q_free[2];         // Q_t's shared memory no longer used by the epilogue
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
@@ -239,8 +238,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == TMA_WARP * 32) {
         mbar_init(&bar_q, 1);
         mbar_init(&bar_q_empty, 1);
-        mbar_init(&bar_k0_full, 1);
-        mbar_init(&bar_k0_empty, 1);
         for (int s = 0; s < C::NP; ++s) {
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_empty[s], 1);
@@ -250,7 +247,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&bar_p_full[t][0], 128);
             mbar_init(&bar_p_full[t][1], 128);
             mbar_init(&bar_o_full[t], 1);
-            mbar_init(&bar_q_free[t], 4);
         }
         mbar_init(&bar_drain, 1);
         abort_flag = 0;
@@ -276,28 +272,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint64_t pol_kv = l2_policy_evict_last();
                 WalkState& walk = walk_sh[TMA_WARP];
                 const Segment& s = seg_sh[TMA_WARP];
-                uint32_t g = 0;        // ring steps issued
-                uint32_t segk = 0;     // segments whose first K was issued
+                uint32_t g = 0;        // ring stages issued
                 bool ok = true;
                 bool skip_k = p.debug_skip_kv_load != 0;  // failure-path test: the first K is never loaded
                 bool dep_done = dep_early;                  // the pre-pass's output may be read
                 while (ok && walk_next(walk, tab, p.plan, static_cast<int>(blockIdx.x), seg_sh[TMA_WARP])) {
                     const SegInfo si = seg_info(p, s);
                     if (si.nmax == 0) continue;
-                    if (segk > 0 && !mbar_wait(&bar_k0_empty, (segk - 1) & 1, limit_ns, &abort_flag)) {
-                        record_failure(&abort_flag, ERRBIT_WAIT_EMPTY);
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&bar_k0_full, C::TILE_BYTES);
-                    if (!skip_k)
-                        for (int bx = 0; bx < C::NB; ++bx)
-                            tma_load_3d_hint(smem + C::OFF_K0 + bx * 16384, &tmK, &bar_k0_full, bx * C::BOX_ELEMS,
-                                             s.k0 * BLOCK_N, si.zkv, pol_kv);
-                    skip_k = false;
-                    ++segk;
+                    // stage 0 of the segment: K_k0 alone; stage i >= 1: V_k0+i-1 and, but for the last,
+                    // K_k0+i
                     const int jend = s.k0 + si.nmax;
-                    for (int j = s.k0; j < jend; ++j) {
+                    for (int j = s.k0 - 1; j < jend; ++j) {
                         const uint32_t st = g % C::NP;
                         if (g >= C::NP &&
                             !mbar_wait(&bar_empty[st], ((g / C::NP) - 1) & 1, limit_ns, &abort_flag)) {
@@ -305,24 +290,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             ok = false;
                             break;
                         }
-                        const bool has_k = j + 1 < jend;
-                        if (!dep_done) {  // the first V tile comes from the pre-pass
+                        const bool has_v = j >= s.k0, has_k = j + 1 < jend;
+                        if (has_v && !dep_done) {  // the first V tile comes from the pre-pass
                             grid_dep_wait();
                             dep_done = true;
                         }
-                        mbar_arrive_expect_tx(&bar_full[st], has_k ? 2 * C::TILE_BYTES : C::TILE_BYTES);
+                        mbar_arrive_expect_tx(&bar_full[st], (has_v ? C::TILE_BYTES : 0) + (has_k ? C::TILE_BYTES : 0));
                         uint8_t* dst = smem + C::OFF_RING + st * C::STAGE_BYTES;
-                        if constexpr (FP8) {  // V^T tile: keys j*128.. (innermost), all d rows
-                            tma_load_3d_hint(dst, &tmV, &bar_full[st], j * BLOCK_N, 0, si.zkv, pol_kv);
-                        } else {
-                            for (int bx = 0; bx < C::NB; ++bx)
-                                tma_load_3d_hint(dst + bx * 16384, &tmV, &bar_full[st], bx * 64, j * BLOCK_N, si.zkv,
-                                                 pol_kv);
+                        if (has_v) {
+                            if constexpr (FP8) {  // V^T tile: keys j*128.. (innermost), all d rows
+                                tma_load_3d_hint(dst, &tmV, &bar_full[st], j * BLOCK_N, 0, si.zkv, pol_kv);
+                            } else {
+                                for (int bx = 0; bx < C::NB; ++bx)
+                                    tma_load_3d_hint(dst + bx * 16384, &tmV, &bar_full[st], bx * 64, j * BLOCK_N,
+                                                     si.zkv, pol_kv);
+                            }
                         }
-                        if (has_k)
+                        if (has_k && !skip_k)
                             for (int bx = 0; bx < C::NB; ++bx)
                                 tma_load_3d_hint(dst + C::TILE_BYTES + bx * 16384, &tmK, &bar_full[st],
                                                  bx * C::BOX_ELEMS, (j + 1) * BLOCK_N, si.zkv, pol_kv);
+                        skip_k = false;
                         ++g;
                     }
                 }
@@ -330,7 +318,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // lands in shared memory after the CTA has exited.
                 if (!ok || abort_flag) {
                     volatile int never = 0;  // these waits must not be cut short by the abort flag
-                    if (segk > 0) (void)mbar_wait(&bar_k0_full, (segk - 1) & 1, limit_ns, &never);
                     for (uint32_t gg = g > C::NP ? g - C::NP : 0; gg < g; ++gg)
                         (void)mbar_wait(&bar_full[gg % C::NP], (gg / C::NP) & 1, limit_ns, &never);
                 }
@@ -347,11 +334,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 while (ok && walk_next(walk, tab, p.plan, static_cast<int>(blockIdx.x), seg_sh[QLOAD_WARP])) {
                     const SegInfo si = seg_info(p, s);
                     if (si.nmax == 0) continue;
-                    // Q_t is reused once the previous segment's MMAs completed and its epilogue
-                    // finished staging output rows there
-                    if (segq > 0 && (!mbar_wait(&bar_q_empty, (segq - 1) & 1, limit_ns, &abort_flag) ||
-                                     !mbar_wait(&bar_q_free[0], (segq - 1) & 1, limit_ns, &abort_flag) ||
-                                     !mbar_wait(&bar_q_free[1], (segq - 1) & 1, limit_ns, &abort_flag))) {
+                    // Q_t is reused once the previous segment's MMAs completed (the epilogue stages its
+                    // output elsewhere, so this load overlaps it)
+                    if (segq > 0 && !mbar_wait(&bar_q_empty, (segq - 1) & 1, limit_ns, &abort_flag)) {
                         record_failure(&abort_flag, ERRBIT_WAIT_EMPTY);
                         ok = false;
                         break;
@@ -385,7 +370,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // Descriptors are built once; a k-step or stage moves the start address, which is the
             // low field (address >> 4) of the descriptor, so offsets are added to it directly.
             const uint64_t dQ = sdesc_sw128(smem_u32(smem), 16, 1024);
-            const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::OFF_K0), 16, 1024);
             const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING + C::TILE_BYTES), 16, 1024);
             // V: MN-major fp16 tile (keys x d), or, fp8, the K-major V^T tile (d rows x 128 keys)
             const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), FP8 ? 16 : 16384, 1024);
@@ -427,22 +411,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             while (ok && next_seg()) {
                 const SegInfo si = seg_info(p, s);
                 if (si.nmax == 0) continue;
-                if (!wait_all(&bar_k0_full, segq & 1, ERRBIT_WAIT_KV) || !wait_all(&bar_q, segq & 1, ERRBIT_WAIT_Q)) {
+                // the segment's first ring stage holds K_k0 alone
+                const uint32_t st0 = g % C::NP;
+                if (!wait_all(&bar_full[st0], (g / C::NP) & 1, ERRBIT_WAIT_KV) ||
+                    !wait_all(&bar_q, segq & 1, ERRBIT_WAIT_Q)) {
                     ok = false;
                     break;
                 }
                 ++segq;
                 tc_fence_after();
                 if (elect_one()) {
+                    const uint64_t dk0 = dRingK + static_cast<uint64_t>((st0 * C::STAGE_BYTES) >> 4);
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
                         if (si.n[t] > 0) {
-                            issue_S(t, dK0);
+                            issue_S(t, dk0);
                             umma_commit(&bar_s_full[t]);
                         }
-                    umma_commit(&bar_k0_empty);
+                    umma_commit(&bar_empty[st0]);
                 }
                 __syncwarp();
+                ++g;
                 for (int jj = 0; jj < si.nmax; ++jj) {
                     const uint32_t st = g % C::NP;
                     if (!wait_all(&bar_full[st], (g / C::NP) & 1, ERRBIT_WAIT_KV)) {
@@ -510,22 +499,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int G = p.plan.G;
         const Segment& s = seg_sh[warp];
         uint32_t cnt_s = 0, cnt_o = 0;  // S_t and O_t phases waited for
-        uint32_t segq = 0;              // segments whose Q the producer loaded (as it counts them)
         bool ok = true;
+        bool staged = false;  // this warp's staging box may still be read by the store engine
 
         while (ok && next_seg()) {
-            // In a segment whose Q the producer loads, this warpgroup may hand Q_t's shared memory
-            // back (bar_q_free) only after that load landed: the producer then waits for exactly one
-            // outstanding q_free phase per tile, even for a tile without keys in the segment.
-            if (seg_info(p, s).nmax > 0) {
-                const bool got = mbar_wait(&bar_q, segq & 1, limit_ns, &abort_flag);
-                ++segq;
-                if (!__all_sync(0xffffffffu, got)) {
-                    if (!got) record_failure(&abort_flag, ERRBIT_WAIT_Q);
-                    ok = false;
-                    break;
-                }
-            }
             // only what the key loop needs stays in registers; the rest is re-read from shared memory
             const int k0 = s.k0;
             const int q0t = s.pair * 2 * BLOCK_M + t * BLOCK_M;
@@ -808,8 +785,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
             }
             const bool live = have && l_run > 0.f;     // this row got weight from this piece
-            // the producer loads Q (and waits for this warpgroup's q_free) only for segments with keys
-            const bool seg_loads_q = seg_info(p, s).nmax > 0;
 
             if (s.kind == SEG_WRITER) {
                 // partial result for the owner of the unit: unnormalised O (row fastest), m, l
@@ -829,16 +804,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 base[(D + 2) * BLOCK_M + r] = static_cast<float>(E);
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) {
-                    flag_release(p.flags + (blockIdx.x * 2 + t) * 4 + wq, 1u);
-                    if (seg_loads_q) mbar_arrive(&bar_q_free[t]);
-                }
+                if (lane == 0) flag_release(p.flags + (blockIdx.x * 2 + t) * 4 + wq, 1u);
                 continue;
             }
-            if (q0t >= p.plan.N) {                      // a tile past the last row: nothing to write
-                if (lane == 0 && seg_loads_q) mbar_arrive(&bar_q_free[t]);
-                continue;
-            }
+            if (q0t >= p.plan.N) continue;  // a tile past the last row: nothing to write
 
             // COMPLETE or OWNER: gather the partial results of the unit's other pieces (owner only)
             const int W = walk_sh[warp].W;
@@ -911,11 +880,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (EXTRA) inv *= p.keep_scale;  // inverted dropout (1 without dropout)
             const bool store = row < p.plan.N;
             const size_t obase = (static_cast<size_t>(bh) * p.plan.N + (store ? row : 0)) * D;
-            const uint32_t stage_base = smem_u32(smem + t * C::TILE_BYTES + wq * C::EPI_BUFS * 4096);
+            // this warp's staging boxes, which the store engine must have read since the warp's last
+            // epilogue (long done by now: a whole segment ran in between)
+            const uint32_t stage_base = smem_u32(smem + C::OFF_EPI + (t * 4 + wq) * C::EPI_BUFS * 4096);
+            if (!OUT_BF16 && staged) {
+                if (lane == 0) bulk_wait_group_read<0>();
+                __syncwarp();
+            }
             // A unit with no other pieces (the usual case) and fp32 output: two chunks per pass, both
             // read from tensor memory together and staged behind one proxy fence; the weight and the
             // normalisation fold into one factor.
-            const bool fast = !OUT_BF16 && C::EPI_BUFS >= 2 && np == 0 && seg_loads_q;
+            const bool fast = !OUT_BF16 && C::EPI_BUFS >= 2 && np == 0;
             if (fast) {
                 const float sc = have ? w_own * inv : 0.f;
 #pragma unroll 1
@@ -992,8 +967,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int i = 0; i < 32; ++i)
                         o[i] = __float_as_uint(fmaf(w2, __ldcg(b2 + (c * 32 + i) * BLOCK_M + r), __uint_as_float(o[i])));
                 }
-                if (OUT_BF16 || !seg_loads_q) {
-                    if (store && OUT_BF16) {
+                if constexpr (OUT_BF16) {
+                    if (store) {
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + obase + c * 32);
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4) {
@@ -1006,20 +981,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                             dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                    } else if (store) {
-                        // (a unit without keys: no staging, its Q region may be in use by the producer)
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + obase + c * 32);
-#pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            dst[v4] = make_float4(
-                                __uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
-                                __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
                     }
                 } else {
                     // fp32 rows leave through the tensor store engine: the warp stages its 32 rows x 32
-                    // columns (128-byte swizzled, 4 KB) in Q_t's shared memory, free since every S_t
-                    // MMA of the segment completed, and one lane stores the box (rows past N are not
-                    // written). Buffers are reused once the store engine has read them.
+                    // columns (128-byte swizzled, 4 KB) in one of its staging boxes and one lane stores
+                    // the box (rows past N are not written). Boxes are reused once the store engine has
+                    // read them.
                     const uint32_t buf = stage_base + (c % C::EPI_BUFS) * 4096;
                     if (c >= C::EPI_BUFS) {
                         if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();
@@ -1045,10 +1012,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float lse = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
                 p.LSE[static_cast<size_t>(bh) * p.plan.N + row] = lse;
             }
-            if (lane == 0 && seg_loads_q) {
-                if (!OUT_BF16) bulk_wait_group_read<0>();  // the staging buffers may be overwritten
-                mbar_arrive(&bar_q_free[t]);
-            }
+            if constexpr (!OUT_BF16) staged = true;
         }
     }
 
