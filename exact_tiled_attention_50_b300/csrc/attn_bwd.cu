@@ -658,21 +658,58 @@ __global__ void __launch_bounds__(Q64_THREADS, 1)
             tc_fence_before();
             mbar_arrive(&bar_sdp_free);  // S^T, dP^T of this step are in registers: the next may land
             uint32_t pp[16], dd[16];
+            // Every one of this thread's 32 (key, query) pairs valid (the key inside kv_len, the queries
+            // below N and, causal, at or after the key): no per-pair mask, the row statistics read as
+            // float4 and the arithmetic two-wide (the same single-rounded fma and product per pair).
+            const bool all_valid = key < kv_valid && q0 + 31 < N && (!p.causal || key <= q0);
+            if (all_valid) {
+                const float4* l4 = reinterpret_cast<const float4*>(lse2);
+                const float4* d4 = reinterpret_cast<const float4*>(dvec);
+                const f32x2 sl2 = make_f32x2(sl, sl);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                float pv[2], dv[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int q = q0 + i + u;
-                    const bool valid = key < kv_valid && q < N && (!p.causal || key <= q);
-                    const float e = valid ? ex2_approx(__uint_as_float(sv[i + u]) * sl - lse2[i + u]) : 0.f;
-                    pv[u] = e;
-                    dv[u] = e * (__uint_as_float(dpv[i + u]) - dvec[i + u]);
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float4 lv = l4[i4], dq = d4[i4];
+                    const int i = 4 * i4;
+                    float x0, x1, x2, x3;
+                    split_f32x2(fma_f32x2(make_f32x2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2,
+                                          make_f32x2(-lv.x, -lv.y)), x0, x1);
+                    split_f32x2(fma_f32x2(make_f32x2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), sl2,
+                                          make_f32x2(-lv.z, -lv.w)), x2, x3);
+                    const f32x2 e01 = make_f32x2(ex2_approx(x0), ex2_approx(x1));
+                    const f32x2 e23 = make_f32x2(ex2_approx(x2), ex2_approx(x3));
+                    const f32x2 g01 = mul_f32x2(e01, add_f32x2(make_f32x2(__uint_as_float(dpv[i]), __uint_as_float(dpv[i + 1])),
+                                                               make_f32x2(-dq.x, -dq.y)));
+                    const f32x2 g23 = mul_f32x2(e23, add_f32x2(make_f32x2(__uint_as_float(dpv[i + 2]), __uint_as_float(dpv[i + 3])),
+                                                               make_f32x2(-dq.z, -dq.w)));
+                    float a0, a1, a2, a3, c0, c1, c2, c3;
+                    split_f32x2(e01, a0, a1);
+                    split_f32x2(e23, a2, a3);
+                    split_f32x2(g01, c0, c1);
+                    split_f32x2(g23, c2, c3);
+                    __nv_bfloat162 ph0 = __floats2bfloat162_rn(a0, a1), ph1 = __floats2bfloat162_rn(a2, a3);
+                    __nv_bfloat162 dh0 = __floats2bfloat162_rn(c0, c1), dh1 = __floats2bfloat162_rn(c2, c3);
+                    pp[2 * i4] = *reinterpret_cast<uint32_t*>(&ph0);
+                    pp[2 * i4 + 1] = *reinterpret_cast<uint32_t*>(&ph1);
+                    dd[2 * i4] = *reinterpret_cast<uint32_t*>(&dh0);
+                    dd[2 * i4 + 1] = *reinterpret_cast<uint32_t*>(&dh1);
                 }
-                __nv_bfloat162 ph = __floats2bfloat162_rn(pv[0], pv[1]);
-                __nv_bfloat162 dh = __floats2bfloat162_rn(dv[0], dv[1]);
-                pp[i / 2] = *reinterpret_cast<uint32_t*>(&ph);
-                dd[i / 2] = *reinterpret_cast<uint32_t*>(&dh);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int q = q0 + i + u;
+                        const bool valid = key < kv_valid && q < N && (!p.causal || key <= q);
+                        const float e = valid ? ex2_approx(__uint_as_float(sv[i + u]) * sl - lse2[i + u]) : 0.f;
+                        pv[u] = e;
+                        dv[u] = e * (__uint_as_float(dpv[i + u]) - dvec[i + u]);
+                    }
+                    __nv_bfloat162 ph = __floats2bfloat162_rn(pv[0], pv[1]);
+                    __nv_bfloat162 dh = __floats2bfloat162_rn(dv[0], dv[1]);
+                    pp[i / 2] = *reinterpret_cast<uint32_t*>(&ph);
+                    dd[i / 2] = *reinterpret_cast<uint32_t*>(&dh);
+                }
             }
             // P^T, dS^T of the previous step must have been consumed by its products
             if (s > 0) {
