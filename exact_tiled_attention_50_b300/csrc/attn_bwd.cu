@@ -44,6 +44,43 @@ constexpr int BW_THREADS = 384;
 constexpr int BW_MMA_WARP = 8;
 constexpr int BW_TMA_WARP = 9;
 
+// P^T and dS^T of one key row over 32 queries whose every pair is valid, as bf16 pairs: P = 2^(s sl -
+// lse2), dS = P (dP - D), with the row statistics read as float4 and the arithmetic two-wide (the same
+// single-rounded fma and product per pair as the masked form).
+__device__ __forceinline__ void bwd_pds_valid32(const uint32_t (&sv)[32], const uint32_t (&dpv)[32], const float* lse2,
+                                                const float* dvec, float sl, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
+    const float4* l4 = reinterpret_cast<const float4*>(lse2);
+    const float4* d4 = reinterpret_cast<const float4*>(dvec);
+    const f32x2 sl2 = make_f32x2(sl, sl);
+#pragma unroll
+    for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 lv = l4[i4], dq = d4[i4];
+        const int i = 4 * i4;
+        float x0, x1, x2, x3;
+        split_f32x2(fma_f32x2(make_f32x2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2,
+                              make_f32x2(-lv.x, -lv.y)), x0, x1);
+        split_f32x2(fma_f32x2(make_f32x2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), sl2,
+                              make_f32x2(-lv.z, -lv.w)), x2, x3);
+        const f32x2 e01 = make_f32x2(ex2_approx(x0), ex2_approx(x1));
+        const f32x2 e23 = make_f32x2(ex2_approx(x2), ex2_approx(x3));
+        const f32x2 g01 = mul_f32x2(e01, add_f32x2(make_f32x2(__uint_as_float(dpv[i]), __uint_as_float(dpv[i + 1])),
+                                                   make_f32x2(-dq.x, -dq.y)));
+        const f32x2 g23 = mul_f32x2(e23, add_f32x2(make_f32x2(__uint_as_float(dpv[i + 2]), __uint_as_float(dpv[i + 3])),
+                                                   make_f32x2(-dq.z, -dq.w)));
+        float a0, a1, a2, a3, c0, c1, c2, c3;
+        split_f32x2(e01, a0, a1);
+        split_f32x2(e23, a2, a3);
+        split_f32x2(g01, c0, c1);
+        split_f32x2(g23, c2, c3);
+        __nv_bfloat162 ph0 = __floats2bfloat162_rn(a0, a1), ph1 = __floats2bfloat162_rn(a2, a3);
+        __nv_bfloat162 dh0 = __floats2bfloat162_rn(c0, c1), dh1 = __floats2bfloat162_rn(c2, c3);
+        pp[2 * i4] = *reinterpret_cast<uint32_t*>(&ph0);
+        pp[2 * i4 + 1] = *reinterpret_cast<uint32_t*>(&ph1);
+        dd[2 * i4] = *reinterpret_cast<uint32_t*>(&dh0);
+        dd[2 * i4 + 1] = *reinterpret_cast<uint32_t*>(&dh1);
+    }
+}
+
 template <int D>
 struct BwCfg {
     static constexpr int NB = D / 64;
@@ -256,6 +293,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 tmem_wait_ld(sv);
                 tmem_wait_ld(dpv);
                 uint32_t pp[16], dd[16];
+                // every pair of the 32 valid: the fast path of the d = 128 kernel (no per-pair mask,
+                // float4 row statistics, two-wide arithmetic)
+                if (key < kv_valid && q0 + c * 32 + 31 < N && (!p.causal || key <= q0 + c * 32))
+                    bwd_pds_valid32(sv, dpv, lse2 + c * 32, dvec + c * 32, sl, pp, dd);
+                else
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     float pv[2], dv[2];
@@ -663,36 +705,7 @@ __global__ void __launch_bounds__(Q64_THREADS, 1)
             // float4 and the arithmetic two-wide (the same single-rounded fma and product per pair).
             const bool all_valid = key < kv_valid && q0 + 31 < N && (!p.causal || key <= q0);
             if (all_valid) {
-                const float4* l4 = reinterpret_cast<const float4*>(lse2);
-                const float4* d4 = reinterpret_cast<const float4*>(dvec);
-                const f32x2 sl2 = make_f32x2(sl, sl);
-#pragma unroll
-                for (int i4 = 0; i4 < 8; ++i4) {
-                    const float4 lv = l4[i4], dq = d4[i4];
-                    const int i = 4 * i4;
-                    float x0, x1, x2, x3;
-                    split_f32x2(fma_f32x2(make_f32x2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2,
-                                          make_f32x2(-lv.x, -lv.y)), x0, x1);
-                    split_f32x2(fma_f32x2(make_f32x2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), sl2,
-                                          make_f32x2(-lv.z, -lv.w)), x2, x3);
-                    const f32x2 e01 = make_f32x2(ex2_approx(x0), ex2_approx(x1));
-                    const f32x2 e23 = make_f32x2(ex2_approx(x2), ex2_approx(x3));
-                    const f32x2 g01 = mul_f32x2(e01, add_f32x2(make_f32x2(__uint_as_float(dpv[i]), __uint_as_float(dpv[i + 1])),
-                                                               make_f32x2(-dq.x, -dq.y)));
-                    const f32x2 g23 = mul_f32x2(e23, add_f32x2(make_f32x2(__uint_as_float(dpv[i + 2]), __uint_as_float(dpv[i + 3])),
-                                                               make_f32x2(-dq.z, -dq.w)));
-                    float a0, a1, a2, a3, c0, c1, c2, c3;
-                    split_f32x2(e01, a0, a1);
-                    split_f32x2(e23, a2, a3);
-                    split_f32x2(g01, c0, c1);
-                    split_f32x2(g23, c2, c3);
-                    __nv_bfloat162 ph0 = __floats2bfloat162_rn(a0, a1), ph1 = __floats2bfloat162_rn(a2, a3);
-                    __nv_bfloat162 dh0 = __floats2bfloat162_rn(c0, c1), dh1 = __floats2bfloat162_rn(c2, c3);
-                    pp[2 * i4] = *reinterpret_cast<uint32_t*>(&ph0);
-                    pp[2 * i4 + 1] = *reinterpret_cast<uint32_t*>(&ph1);
-                    dd[2 * i4] = *reinterpret_cast<uint32_t*>(&dh0);
-                    dd[2 * i4 + 1] = *reinterpret_cast<uint32_t*>(&dh1);
-                }
+                bwd_pds_valid32(sv, dpv, lse2, dvec, sl, pp, dd);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
