@@ -403,3 +403,48 @@ def attention_bias_dropout_np(q, k, v, scale, bias=None, p=0.0, seed=0, offset=0
     if return_p:
         return O, LSE, P_all
     return O, LSE
+
+
+def attention_bias_dropout_rows_np(q, k, v, scale, b, h, rows, bias_rows=None, p=0.0, seed=0, offset=0,
+                                   causal=False, kv_len=None):
+    """O [len(rows), d], LSE [len(rows)] of attention_bias_dropout_np for the query rows `rows` of head
+    (b, h) alone, each row over all N keys: the same definition restricted to those rows, for sizes whose
+    full [B, H, N, N] scores and mask do not fit on the host. bias_rows: None or the rows' biases
+    [len(rows), N] (natural-log units). The keep decisions of row i come from the same Philox4x32-10
+    counters (j >> 3, i, b * H + h, offset) as dropout_keep_mask."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, N, d = q.shape
+    kvh = h // (H // k.shape[1])
+    L = N if kv_len is None else int(kv_len[b])
+    t = dropout_threshold(p)
+    inv_keep = 65536.0 / (65536.0 - t)
+    G = (N + 7) // 8
+    key = np.array([int(seed) & 0xFFFFFFFF, (int(seed) >> 32) & 0xFFFFFFFF], np.uint64)
+    O = np.zeros((len(rows), d))
+    LSE = np.zeros(len(rows))
+    for n, i in enumerate(rows):
+        s = float(scale) * (k[b, kvh] @ q[b, h, i])
+        if bias_rows is not None:
+            s = s + np.asarray(bias_rows[n], dtype=np.float64)
+        jk = np.arange(N)  # row i of key_mask: keys below kv_len (and, causal, not after the query)
+        s = np.where((jk < max(0, min(L, N))) & ((jk <= i) if causal else True), s, -np.inf)
+        m = s.max()
+        if not np.isfinite(m):
+            O[n] = 0.0
+            LSE[n] = -np.inf
+            continue
+        e = np.exp(s - m)
+        l = e.sum()
+        if t > 0:
+            ctr = np.stack([np.arange(G), np.full(G, i), np.full(G, b * H + h), np.full(G, int(offset) & 0xFFFFFFFF)],
+                           axis=-1).astype(np.uint64)
+            w = philox4x32_10(ctr, np.broadcast_to(key, (G, 2))).astype(np.uint32)    # [G, 4]
+            u = np.stack([w & 0xFFFF, w >> 16], axis=-1).reshape(G * 8)[:N]          # u_(j mod 8) of group j >> 3
+            keep = u >= t
+        else:
+            keep = np.ones(N, bool)
+        O[n] = ((e / l) * keep * inv_keep) @ v[b, kvh]
+        LSE[n] = m + np.log(l)
+    return O, LSE

@@ -111,3 +111,33 @@ def test_keep_decisions_exactly():
         j = target[h]
         got = O[0, h, np.arange(N), j % d] * (1 - t / 65536.0) / (j + 1)  # 1 if kept, 0 if dropped
         np.testing.assert_allclose(got, keep[0, h, np.arange(N), j].astype(np.float64), rtol=0, atol=1e-3)
+
+
+@pytest.mark.parametrize("with_bias", [True, False])
+def test_full_size_sampled_rows(with_bias):
+    """The bench's bias + dropout and dropout-only workloads as bench.py times them: B1 H16 N8192 d128
+    (peaky keys), a full [B, H, N, N] bf16 bias drawn on the device with the bench's seed, p = 0.1,
+    seed 1, offset 0. Rows sampled in four heads (tile edges and random rows), each checked element by
+    element against the row-restricted oracle with the forward's bar; every keep decision of a sampled
+    row enters its output."""
+    from exact_tiled_attention_50_b300 import attn
+    x = inputs.make_inputs(inputs.WORKLOADS[inputs.HEADLINE])
+    B, H, N, d = x.q.shape
+    bias = None
+    if with_bias:
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(inputs.SEED_BASE + 4000)
+        bias = torch.randn((B, H, N, N), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    O, L = attn.attn_fwd_ex(x.q.cuda(), x.k.cuda(), x.v.cuda(), scale=x.scale, bias=bias, dropout_p=0.1, seed=1,
+                            offset=0)
+    rc = attn.check()
+    assert rc == attn.ATTN_OK, attn.status_string(rc)
+    q, k, v = x.q.double().numpy(), x.k.double().numpy(), x.v.double().numpy()
+    rng = np.random.default_rng(17)
+    for h in (0, 5, 10, 15):
+        rows = np.unique(np.concatenate([[0, 127, 128, N - 1], rng.integers(0, N, 12)]))
+        bias_rows = None if bias is None else bias[0, h, torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
+        Or, Lr = o.attention_bias_dropout_rows_np(q, k, v, x.scale, 0, h, rows, bias_rows=bias_rows, p=0.1, seed=1,
+                                                  offset=0)
+        parity.compare(O[0, h, torch.as_tensor(rows, device="cuda")], L[0, h, torch.as_tensor(rows, device="cuda")],
+                       Or, Lr, "bf16", what=f"{'bias + ' if with_bias else ''}dropout, head {h}")

@@ -192,3 +192,24 @@ def test_unmutated_copy_passes():
 @pytest.mark.parametrize("name", list(MUTANTS))
 def test_planted_mistake_is_caught(name):
     assert _checks_fail(_mutant(*MUTANTS[name])), name
+
+
+@pytest.mark.parametrize("causal,kv_len", [(False, None), (True, [37, 50])])
+def test_row_restricted_oracle_equals_the_full_one(causal, kv_len):
+    """attention_bias_dropout_rows_np (the full-size tests' per-row oracle) against the whole-matrix
+    attention_bias_dropout_np: every row of every head, with a bias, dropout, GQA, causal and padding."""
+    rng = np.random.default_rng(11)
+    B, H, H_kv, N, d = 2, 4, 2, 50, 16
+    q, k, v = rng.standard_normal((B, H, N, d)), rng.standard_normal((B, H_kv, N, d)), rng.standard_normal((B, H_kv, N, d))
+    bias = rng.standard_normal((B, H, N, N)) * 2.0
+    bias[0, 1, :, 5:9] = -np.inf
+    lens = None if kv_len is None else np.array(kv_len)
+    O, L = o.attention_bias_dropout_np(q, k, v, 0.3, bias=bias, p=0.3, seed=2 ** 33 + 9, offset=4, causal=causal,
+                                       kv_len=lens)
+    rows = np.arange(N)
+    for b in range(B):
+        for h in range(H):
+            Or, Lr = o.attention_bias_dropout_rows_np(q, k, v, 0.3, b, h, rows, bias_rows=bias[b, h], p=0.3,
+                                                      seed=2 ** 33 + 9, offset=4, causal=causal, kv_len=lens)
+            np.testing.assert_allclose(Or, O[b, h], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(Lr, L[b, h], rtol=0, atol=1e-12)
