@@ -274,3 +274,58 @@ def test_host_pipeline_matches_the_oracle(B, H, H_kv, N, d, dtype, causal, padde
     O_ref, L_ref = oracle.attention(x.q, x.k, x.v, x.scale, causal=causal, kv_len=x.kv_len)
     parity.compare(oh, lh, O_ref, L_ref, dtype, what=f"host pipeline {B}x{H}/{H_kv} N={N} groups={n_groups}")
     assert torch.equal(od.cpu(), oh)  # the device buffers hold the same result
+
+
+def test_host_pipeline_full_size_sampled_rows():
+    """attn_fwd_host on the bench workload (B1 H16 N8192 d128, the end-to-end leg's call with its default
+    tapered head groups): sampled rows of every head against the oracle, and the whole host result within
+    twice the forward's bar of attn_fwd's on the device inputs. The two need not agree bit for bit: a
+    group of one or two heads gets its own schedule, in which the persistent kernel splits the units
+    into pieces merged in fp32 (shorter tensor-core accumulations, slightly different rounding)."""
+    import oracle
+    from exact_tiled_attention_50_b300 import attn
+    x = inputs.make_inputs(inputs.WORKLOADS[inputs.HEADLINE])
+    B, H, N, d = x.q.shape
+    qh, kh, vh = x.q.pin_memory(), x.k.pin_memory(), x.v.pin_memory()
+    oh = torch.full((B, H, N, d), float("nan"), dtype=torch.float32).pin_memory()
+    lh = torch.full((B, H, N), float("nan"), dtype=torch.float32).pin_memory()
+    qd, kd, vd = torch.empty_like(x.q, device="cuda"), torch.empty_like(x.k, device="cuda"), torch.empty_like(x.v, device="cuda")
+    od = torch.empty((B, H, N, d), dtype=torch.float32, device="cuda")
+    ld = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    attn.attn_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, scale=x.scale)
+    torch.cuda.synchronize()
+    assert attn.check() == attn.ATTN_OK
+    rows = parity.sample_rows(B, H, N, None, per_head=24, seed=5)
+    O_ref, L_ref = oracle.attention_rows(x.q, x.k, x.v, x.scale, rows)
+    parity.compare(oh.reshape(-1, d)[torch.as_tensor(rows)], lh.reshape(-1)[torch.as_tensor(rows)], O_ref, L_ref,
+                   "bf16", what="host pipeline, bench workload")
+    O2, L2 = attn.attn_fwd(x.q.cuda(), x.k.cuda(), x.v.cuda(), scale=x.scale)
+    assert float((O2.cpu() - oh).abs().max()) <= 2 * parity.TOL["bf16"]["max_abs"]
+    assert float((L2.cpu() - lh).abs().max()) <= 2 * parity.LSE_TOL
+
+
+def test_bf16_output_full_size_sampled_rows():
+    """bf16 output on the bench workload (B1 H16 N8192 d128): its epilogue rounds O to bf16 straight from
+    the registers; sampled rows against the oracle with the bar widened by half an output ulp."""
+    x = inputs.make_inputs(inputs.WORKLOADS[inputs.HEADLINE])
+    parity.check_sampled(x, "bf16", per_head=24, out_dtype=torch.bfloat16, what="bf16 out, bench workload", seed=9)
+
+
+@pytest.mark.parametrize("name,heads", [("sweep_b1h16_d128_n8192_noncausal_peaky", (0, 9)),
+                                        ("sweep_b1h16_d128_n16384_causal_peaky", (3, 12))])
+def test_whole_heads_at_the_longest_sizes(name, heads):
+    """Every element of two whole heads at N = 8192 and 16384 (peaky keys) against the oracle: the
+    largest errors sit in single rows dominated by one key (fp16 P rounding plus the tensor core's long
+    accumulation), which row sampling may miss."""
+    import oracle
+    from exact_tiled_attention_50_b300 import attn
+    w = inputs.WORKLOADS[name]
+    x = inputs.make_inputs(w)
+    B, H, N, d = x.q.shape
+    O, L = attn.attn_fwd(x.q.cuda(), x.k.cuda(), x.v.cuda(), scale=x.scale, causal=w.causal)
+    rc = attn.check()
+    assert rc == attn.ATTN_OK, attn.status_string(rc)
+    for h in heads:
+        rows = np.arange(h * N, (h + 1) * N, dtype=np.int64)
+        O_ref, L_ref = oracle.attention_rows(x.q, x.k, x.v, x.scale, rows, causal=w.causal)
+        parity.compare(O[0, h], L[0, h], O_ref, L_ref, "bf16", what=f"{name} head {h}, every row")
