@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             int E = 0;
             float m_run = -INFINITY;                   // reference maximum (log2 domain, already scaled)
-            float l_run = 0.f;                         // running sum of exp2(s*sl - m_run)
+            float l_run = 0.f;                         // running sum of exp2(s*sl - m_run), as P V uses them
 
             for (int jj = 0; jj < nkvt; ++jj) {
                 const int j = k0 + jj;
@@ -707,21 +707,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 const float m_sub = (m_run == -INFINITY) ? 0.f : m_run;
-                // P = exp2(s * scale*log2e - m), written to TMEM as fp16 pairs over the first 64 columns
-                // of S_t, one half (64 keys) at a time; each half is announced as soon as it is stored.
-                // The scale-and-subtract and the row sum use two-wide fp32 instructions. A tile whose
-                // V exponent is below E enters as P * 2^(e_j - E) (folded into the exponent); the row
-                // sum takes P itself.
+                // P = exp2(s * scale*log2e - m), written to TMEM as fp16 pairs (E4M3 quadruples) over the
+                // first 64 (32) columns of S_t, one half (64 keys) at a time; each half is announced as
+                // soon as it is stored. The scale-and-subtract (and fp8's row sum) use two-wide fp32
+                // instructions. A tile whose V exponent is below E enters as P * 2^(e_j - E) (folded into
+                // the exponent); the row sums take P itself.
+                // The row sum (O's divisor and the LSE's sum) takes P as the P V product uses it: rounded
+                // to fp16 and before dropout. A row dominated by one key then divides that key's rounding
+                // out of O instead of keeping it (up to 2^-12 |V| otherwise), and O, LSE stay consistent
+                // for a merge of partial results. It is taken from the packed pairs after both halves are
+                // handed over, while the warpgroup waits for its next S (with dropout, in the loop,
+                // before the draws zero some of P). fp8 sums its fp32 exponentials in the loop (its
+                // E4M3 rounding, 2^-4, would move the LSE too far).
                 {
                     const int shift = e_j - E;  // <= 0, almost always 0
                     const f32x2 sl2 = make_f32x2(slj, slj);
                     const f32x2 nm2 = make_f32x2(static_cast<float>(shift) - m_sub, static_cast<float>(shift) - m_sub);
                     f32x2 acc0 = make_f32x2(0.f, 0.f), acc1 = acc0;
+                    float q0 = 0.f, q1 = 0.f, q2 = 0.f, q3 = 0.f;  // the fp16 row sum of this tile, four chains
+                    uint32_t pk[2][FP8 ? 16 : 32];  // both halves' P, kept for the deferred row sum
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         if constexpr (FP8) {
                             // E4M3, four keys per TMEM column: 16 columns per half
-                            uint32_t pk[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 float e0, e1, e2, e3;
@@ -734,11 +742,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 e3 = ex2_approx(e3);
                                 acc0 = add_f32x2(acc0, make_f32x2(e0, e1));
                                 acc1 = add_f32x2(acc1, make_f32x2(e2, e3));
-                                pk[i] = pack_e4m3x4(e0, e1, e2, e3);
+                                pk[half][i] = pack_e4m3x4(e0, e1, e2, e3);
                             }
-                            tmem_st16(tS + 16 * half, pk);
+                            tmem_st16(tS + 16 * half, pk[half]);
                         } else {
-                            uint32_t pk[32];
                             uint4 rnd = make_uint4(0u, 0u, 0u, 0u);  // dropout draws of 8 keys
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
@@ -746,12 +753,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 split_f32x2(
                                     fma_f32x2(make_f32x2(x[64 * half + 2 * i], x[64 * half + 2 * i + 1]), sl2, nm2),
                                     e0, e1);
-                                e0 = ex2_approx(e0);
-                                e1 = ex2_approx(e1);
-                                const f32x2 e = make_f32x2(e0, e1);
-                                if (i & 1) acc1 = add_f32x2(acc1, e);  // the row sum takes P before dropout
-                                else acc0 = add_f32x2(acc0, e);
+                                pk[half][i] = pack_f16x2(ex2_approx(e0), ex2_approx(e1));
                                 if constexpr (EXTRA) {
+                                    if (i & 1) {
+                                        q2 = add_f16lo(q2, pk[half][i]);
+                                        q3 = add_f16hi(q3, pk[half][i]);
+                                    } else {
+                                        q0 = add_f16lo(q0, pk[half][i]);
+                                        q1 = add_f16hi(q1, pk[half][i]);
+                                    }
                                     if (p.drop_t != 0u) {
                                         // keys 2i, 2i+1 of this half: word (i mod 4) of the draws of their
                                         // group of 8, low half for the even key, high half for the odd one
@@ -763,22 +773,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                 p.round_key);
                                         const uint32_t w = (i & 3) == 0 ? rnd.x : (i & 3) == 1 ? rnd.y
                                                          : (i & 3) == 2 ? rnd.z : rnd.w;
-                                        if ((w & 0xffffu) < p.drop_t) e0 = 0.f;
-                                        if ((w >> 16) < p.drop_t) e1 = 0.f;
+                                        if ((w & 0xffffu) < p.drop_t) pk[half][i] &= 0xffff0000u;  // +0, low half
+                                        if ((w >> 16) < p.drop_t) pk[half][i] &= 0x0000ffffu;
                                     }
                                 }
-                                pk[i] = pack_f16x2(e0, e1);
                             }
-                            tmem_st32(tS + 32 * half, pk);
+                            tmem_st32(tS + 32 * half, pk[half]);
                         }
                         tmem_wait_st();
                         tc_fence_before();
                         mbar_arrive(&bar_p_full[t][half]);
                     }
-                    float s0, s1, s2, s3;
-                    split_f32x2(acc0, s0, s1);
-                    split_f32x2(acc1, s2, s3);
-                    const float psum = (s0 + s1) + (s2 + s3);
+                    if constexpr (!FP8 && !EXTRA) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half)
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                q0 = add_f16lo(q0, pk[half][i]);
+                                q1 = add_f16hi(q1, pk[half][i]);
+                                q2 = add_f16lo(q2, pk[half][i + 1]);
+                                q3 = add_f16hi(q3, pk[half][i + 1]);
+                            }
+                    }
+                    float psum;
+                    if constexpr (FP8) {
+                        float s0, s1, s2, s3;
+                        split_f32x2(acc0, s0, s1);
+                        split_f32x2(acc1, s2, s3);
+                        psum = (s0 + s1) + (s2 + s3);
+                    } else {
+                        psum = (q0 + q1) + (q2 + q3);
+                    }
                     l_run += shift == 0 ? psum : ldexpf(psum, -shift);
                 }
             }

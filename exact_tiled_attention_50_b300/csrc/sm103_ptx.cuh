@@ -461,4 +461,17 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return d;
 }
 
+// acc + the fp16 value in the low / high half of p, as one mixed-precision add (the fp16 operand is
+// widened exactly, the sum rounded to nearest in fp32).
+__device__ __forceinline__ float add_f16lo(float acc, uint32_t p) {
+    float d;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.f16 %0, l, %2;\n\t}" : "=f"(d) : "r"(p), "f"(acc));
+    return d;
+}
+__device__ __forceinline__ float add_f16hi(float acc, uint32_t p) {
+    float d;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.f16 %0, h, %2;\n\t}" : "=f"(d) : "r"(p), "f"(acc));
+    return d;
+}
+
 }  // namespace attn_sm103

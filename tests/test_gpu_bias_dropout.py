@@ -76,7 +76,11 @@ def test_no_bias_no_dropout_equals_attn_fwd():
     O, L, O_ref, L_ref = _run(x)
     parity.compare(O, L, O_ref, L_ref, "bf16", what="plain")
     O2, L2 = attn.attn_fwd(x.q.cuda(), x.k.cuda(), x.v.cuda(), scale=x.scale, causal=True)
-    assert torch.allclose(O, O2, rtol=0, atol=2e-3) and torch.allclose(L, L2, rtol=0, atol=1e-5)
+    # the two kernels form the scaled scores with different roundings (the bias variant adds its bias
+    # to S * scale*log2e), which can flip the fp16 rounding of a probability, and the row sum takes the
+    # rounded values: O and LSE then agree within the forward's bars, not bit for bit
+    assert torch.allclose(O, O2, rtol=0, atol=parity.TOL["bf16"]["max_abs"])
+    assert torch.allclose(L, L2, rtol=0, atol=parity.LSE_TOL)
 
 
 def test_split_units_of_the_persistent_schedule():
